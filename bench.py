@@ -1,0 +1,448 @@
+"""Throughput of non-causal DiT attention on GB300: fused pass and p-chunk ring decomposition.
+
+One step = the whole hot path once over one batch of synthetic input: the
+fused attention pass (dit_attn_fwd) and the same attention as p KV chunks
+(p x dit_attn_chunk_fwd, one per virtual ring rank) merged by
+dit_attn_lse_merge.  FLOPs counted per pass: 4*B*H*N^2*D (the two GEMMs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan22] [--impl reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (weak scaling, no data-path collective); the timed
+region is bracketed by a barrier + synchronize and the max over ranks is used.
+`--impl reference` times the fp64 CPU oracle (the only reference this path
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from diffusion_transformer_long_gb300 import synth  # noqa: E402
+
+METRIC = "attention TFLOP/s & % of GB300 BF16 dense peak (H=24,N=27280,D=128)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129e6
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_kernel.cuh", "sm103_ptx.cuh", "attn_fwd.cu"):
+        with open(os.path.join(ROOT, "diffusion_transformer_long_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if the
+    summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    digest = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    traffic = re.search(r"dram_bytes_per_launch_full_size:\s*([0-9.eE+]+)", text)
+    if not digest or not traffic or digest.group(1) != kernel_source_digest():
+        return None
+    return float(traffic.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device_index)
+        self.cmd = ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", "200"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        rows = []
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names[1:], r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        watts = []
+        for r in rows:
+            try:
+                watts.append(float(r[2]))
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(watts) if watts else None}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, rank, world, local
+    return None, 0, 1, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def oracle_sample_tflops(w, q, k, v, target_s: float, rows_cap: int = 100000):
+    """Times the fp64 oracle on a bounded row sample of workload w (all heads, R query rows).
+    Returns (tflops, seconds, rows_per_head, threads)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0))
+    heads = w.B * w.H
+    # calibrate on 2 rows per head
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, rows=list(range(2)), threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_row = dt / (2 * heads)
+    R = int(max(2, min(rows_cap, target_s / (per_row * heads))))
+    R = min(R, w.N)
+    rows = synth.sample_rows(w.N, R, edge=min(16, R // 2), seed=w.seed)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, w.scale, rows=rows, threads=threads)
+    secs = time.perf_counter() - t0
+    flops = 4.0 * heads * len(rows) * w.N * w.D
+    used = oracle.threads_used(threads, heads * len(rows))
+    return flops / secs / 1e12, secs, len(rows), used
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle on bounded samples of the same workload."""
+    dist, rank, world, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    q, k, v = synth.make_qkv(w)
+    per_step = []
+    rows_used = threads = 0
+    for i in range(args.warmup + args.steps):
+        tf, secs, rows_used, threads = oracle_sample_tflops(w, q, k, v, target_s=args.ref_step_s)
+        if i >= args.warmup:
+            per_step.append((tf, secs))
+    value = statistics.median(t for t, _ in per_step)
+    ms = statistics.median(s for _, s in per_step) * 1e3
+    sample = (f"{w.B * w.H} heads x {rows_used} query rows against all {w.N} keys per step "
+              f"(fp64 oracle, one step ~{args.ref_step_s:.0f} s)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; no dataset exists for this path)",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: B={w.B} H={w.H} N={w.N} D={w.D} bf16 Q/K/V, non-causal, "
+                        f"fused pass + p={w.p} KV chunks ({'/'.join(map(str, sorted(set(w.chunks))))})"
+                        f" merged by LSE",
+            "B": w.B, "H": w.H, "N": w.N, "D": w.D, "p": w.p, "chunks": list(w.chunks),
+            "out_dtype": "fp32", "partial_dtype": "fp32",
+            "l2": f"no flush: Q/K/V are {3 * w.B * w.H * w.N * w.D * 2 / 1e6:.0f} MB "
+                  f"(> {L2_BYTES / 1e6:.0f} MB L2)" if 3 * w.B * w.H * w.N * w.D * 2 > L2_BYTES
+                  else "L2 flushed between steps (256 MB write)",
+            "parallelism": "replicas (one independent workload per GPU)"}
+
+
+def run_gpu(args):
+    from diffusion_transformer_long_gb300 import ditattn as da
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    q_h, k_h, v_h = synth.make_qkv(w)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    B, H, N, D, p = w.B, w.H, w.N, w.D, w.p
+    out_f = torch.empty((B, H, N, D), device=dev, dtype=torch.float32)
+    lse_f = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    parts = torch.empty((p, B, H, N, D), device=dev, dtype=torch.float32)
+    lses = torch.empty((p, B, H, N), device=dev, dtype=torch.float32)
+    out_c = torch.empty_like(out_f)
+    lse_c = torch.empty_like(lse_f)
+    starts = synth.chunk_starts(w.chunks)
+    small = 3 * B * H * N * D * 2 <= L2_BYTES
+    flush = torch.empty(int(256e6) // 4, device=dev, dtype=torch.float32) if small else None
+    stream = torch.cuda.current_stream(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    fused_ev, merge_ev, chunk_ev = [], [], []
+
+    def step(record=False):
+        if record:
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+        da.attn_fwd(q, k, v, out=out_f, lse=lse_f, scale=w.scale)
+        if record:
+            e1.record(stream)
+            fused_ev.append((e0, e1))
+            c0 = ev()
+            c0.record(stream)
+        for c, (s, n) in enumerate(zip(starts, w.chunks)):
+            da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=parts[c], lse=lses[c],
+                              scale=w.scale)
+        if record:
+            m0, m1 = ev(), ev()
+            m0.record(stream)
+        da.attn_lse_merge(parts, lses, out=out_c, lse=lse_c)
+        if record:
+            m1.record(stream)
+            merge_ev.append((m0, m1))
+            chunk_ev.append((c0, m1))
+
+    launches_per_step = 1 + p + 1
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    diff = (out_f - out_c).abs().max().item()
+
+    # ---- timed region (device clock) ----
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        t0, t1 = ev(), ev()
+        if flush is None:
+            t0.record(stream)
+            for _ in range(args.steps):
+                step(record=True)
+            t1.record(stream)
+            torch.cuda.synchronize(dev)
+            elapsed_ms = t0.elapsed_time(t1)
+        else:
+            elapsed_ms = 0.0
+            for _ in range(args.steps):
+                flush.zero_()
+                s0, s1 = ev(), ev()
+                s0.record(stream)
+                step(record=True)
+                s1.record(stream)
+                torch.cuda.synchronize(dev)
+                elapsed_ms += s0.elapsed_time(s1)
+        barrier(dist)
+    da.check(dev)
+    ms_step = max_over_ranks(dist, elapsed_ms / args.steps)
+    fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fused_ev)
+    merge_ms = statistics.mean(a.elapsed_time(b) for a, b in merge_ev)
+    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in chunk_ev)
+    fused_ms = max_over_ranks(dist, fused_ms)
+    chunk_ms = max_over_ranks(dist, chunk_ms)
+    merge_ms = max_over_ranks(dist, merge_ms)
+    step_flops = 2 * w.flops  # the fused pass and the chunked pass each compute the attention
+    value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    o1_h = torch.empty(out_f.shape, dtype=torch.float32, pin_memory=True)
+    l1_h = torch.empty(lse_f.shape, dtype=torch.float32, pin_memory=True)
+    o2_h = torch.empty(out_f.shape, dtype=torch.float32, pin_memory=True)
+    l2_h = torch.empty(lse_f.shape, dtype=torch.float32, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (q_p, k_p, v_p))
+    d2h = sum(t.numel() * t.element_size() for t in (o1_h, l1_h, o2_h, l2_h))
+
+    def e2e_step():
+        qd = q_p.to(dev, non_blocking=True)
+        kd = k_p.to(dev, non_blocking=True)
+        vd = v_p.to(dev, non_blocking=True)
+        o1, l1 = da.attn_fwd(qd, kd, vd, scale=w.scale)
+        o2, l2 = da.chunk_attention(qd, kd, vd, w.chunks, scale=w.scale)
+        o1_h.copy_(o1, non_blocking=True)
+        l1_h.copy_(l1, non_blocking=True)
+        o2_h.copy_(o2, non_blocking=True)
+        l2_h.copy_(l2, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, args.steps // 4)
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    da.check(dev)
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / e2e_steps)
+    e2e_value = step_flops * world / (e2e_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak_sust = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    peak_burst = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    fused_tflops = w.flops / (fused_ms * 1e-3) / 1e12
+    chunk_tflops = w.flops / (chunk_ms * 1e-3) / 1e12
+    merge_bytes = p * B * H * N * (D * 4 + 4) + B * H * N * (D * 4 + 4)
+    merge_gbs = merge_bytes / (merge_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(w.name)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            tf, secs, rows, threads = oracle_sample_tflops(w, q_h, k_h, v_h,
+                                                           target_s=args.cpu_baseline_s)
+            cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+                   "sample": f"{B * H} heads x {rows} query rows against all {N} keys "
+                             f"({secs:.1f} s of fp64 oracle)"}
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V shaped like Wan2.2 TI2V-5B attention)",
+            "config": workload_config(w),
+            "fraction_of_peak": fused_tflops / peak_sust,
+            "paths": {
+                "fused": {"ms": fused_ms, "tflops": fused_tflops},
+                "chunk_merge": {"ms": chunk_ms, "tflops": chunk_tflops,
+                                "ratio_to_fused": chunk_ms / fused_ms,
+                                "merge_ms": merge_ms, "merge_gbs": merge_gbs,
+                                "merge_frac_of_hbm": merge_gbs / hbm},
+                "fused_vs_chunk_max_abs": diff,
+            },
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,fp32>",
+                         "achieved": fused_tflops, "peak": peak_sust, "unit": "TFLOP/s",
+                         "frac": fused_tflops / peak_sust,
+                         "peak_kind": f"{peak_src} bf16 sustained",
+                         "frac_of_burst_peak": fused_tflops / peak_burst,
+                         "traffic": traffic,
+                         "algorithmic_bytes": 4 * B * H * N * D * 2 + B * H * N * (D * 4 + 4)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+    if dist is not None:
+        dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="wan22", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
+    ap.add_argument("--ref-step-s", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

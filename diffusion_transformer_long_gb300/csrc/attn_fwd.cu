@@ -1,0 +1,92 @@
+// Host side of the attention kernel: TMA descriptor encoding and launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "attn_kernel.cuh"
+#include "launch.h"
+
+namespace ditattn {
+namespace {
+
+// Test-only failure injection (dit_test_inject_stall).
+int g_stall_kv = 0;
+long long g_wait_limit = kDefaultWaitLimit;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 3-D bf16 map (d, rows, heads) with 128-row x 64-column boxes and 128-byte
+// swizzle; rows past `rows` read as zero.
+bool encode_bhnd(CUtensorMap* m, const void* base, int d, int rows, int heads,
+                 long long head_stride_elems) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(head_stride_elems) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockM), 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool kF32>
+cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
+  constexpr int kSmem = AttnSmem<D>::kBytes;
+  auto kern = attn_fwd_kernel<D, kF32>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(static_cast<unsigned>(prm.q_pairs) * static_cast<unsigned>(prm.bh_count));
+  kern<<<grid, kThreads, kSmem, st>>>(prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
+  AttnParams prm;
+  if (!encode_bhnd(&prm.tm_q, a.q, a.d, a.n_q, a.bh, a.q_head_stride) ||
+      !encode_bhnd(&prm.tm_k, a.k, a.d, a.n_kv, a.bh, a.kv_head_stride) ||
+      !encode_bhnd(&prm.tm_v, a.v, a.d, a.n_kv, a.bh, a.kv_head_stride))
+    return cudaErrorInvalidValue;
+  prm.out = a.out;
+  prm.lse = a.lse;
+  prm.status = a.status;
+  prm.n_q = a.n_q;
+  prm.n_kv = a.n_kv;
+  prm.bh_count = a.bh;
+  prm.q_pairs = (a.n_q + 2 * kBlockM - 1) / (2 * kBlockM);
+  prm.scale_log2 = a.scale * 1.4426950408889634f;
+  prm.wait_limit = g_wait_limit;
+  prm.stall_kv = g_stall_kv;
+  if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
+  return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);
+}
+
+void set_stall_injection(int enable, long long wait_limit_cycles) {
+  g_stall_kv = enable ? 1 : 0;
+  g_wait_limit = wait_limit_cycles > 0 ? wait_limit_cycles : kDefaultWaitLimit;
+}
+
+}  // namespace ditattn

@@ -1,0 +1,242 @@
+"""Python binding of the ditattn C ABI (include/ditattn.h): argument marshalling only.
+
+Every step of attention runs in the library's CUDA kernels; this module checks
+shapes/dtypes, allocates outputs with PyTorch when the caller does not pass
+them, and hands raw pointers plus the current CUDA stream to the C entry
+points.  There is no CPU fallback: without the built library or a CUDA device
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
+DIT_F32, DIT_BF16 = 0, 1
+
+EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_chunk_fwd", "dit_attn_lse_merge", "dit_attn_check",
+                    "dit_test_inject_stall", "dit_status_string", "dit_version")
+
+_lib = None
+
+
+class DitError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libditattn.so (built in-tree by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(path)
+        P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+        L.dit_attn_fwd.restype = I
+        L.dit_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
+        L.dit_attn_chunk_fwd.restype = I
+        L.dit_attn_chunk_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, P]
+        L.dit_attn_lse_merge.restype = I
+        L.dit_attn_lse_merge.argtypes = [P, P, I, P, P, I, I, I, I, I, I, P]
+        L.dit_attn_check.restype = I
+        L.dit_attn_check.argtypes = [P]
+        L.dit_test_inject_stall.restype = None
+        L.dit_test_inject_stall.argtypes = [I, LL]
+        L.dit_status_string.restype = ctypes.c_char_p
+        L.dit_status_string.argtypes = [I]
+        L.dit_version.restype = I
+        L.dit_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().dit_status_string(int(status)).decode()
+
+
+def _dt(dtype: torch.dtype) -> int:
+    if dtype == torch.float32:
+        return DIT_F32
+    if dtype == torch.bfloat16:
+        return DIT_BF16
+    raise TypeError(f"unsupported output dtype {dtype}; use torch.float32 or torch.bfloat16")
+
+
+def _stream(device: torch.device, stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, D]")
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [B, H, N, D]")
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, stream=None):
+    """Fused attention over all keys.  q, k, v: CUDA bf16 [B, H, N, D] contiguous.
+
+    Returns (out [B, H, N, D] of out_dtype, lse fp32 [B, H, N]).
+    """
+    _check_qkv(q, k, v)
+    if not (k.is_contiguous() and v.is_contiguous()) or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("k and v must be contiguous with q's shape")
+    B, H, N, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, N, D), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
+                                scale, _dt(out.dtype), _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_fwd")
+    return out, lse
+
+
+def kv_head_stride(k: torch.Tensor) -> int:
+    """Elements between consecutive (b, h) heads of a [B, H, n, D] K/V view (rows D apart)."""
+    B, H, n, D = k.shape
+    if k.stride(3) != 1 or (n > 1 and k.stride(2) != D):
+        raise ValueError("K/V rows must be contiguous and D elements apart")
+    if B > 1 and H > 1:
+        if k.stride(0) != H * k.stride(1):
+            raise ValueError("K/V heads must be evenly spaced across the batch")
+        return k.stride(1)
+    if H > 1:
+        return k.stride(1)
+    if B > 1:
+        return k.stride(0)
+    return n * D  # a single head: the stride is never used
+
+
+def attn_chunk_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, stream=None):
+    """Attention of q against one KV chunk (a view such as k[:, :, s:s+n] or a packed buffer).
+
+    Returns (partial out [B, H, N_q, D] of out_dtype, lse fp32 [B, H, N_q]).
+    """
+    _check_qkv(q, k, v)
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v chunk must be [B, H, n_kv, D] matching q")
+    hs = kv_head_stride(k)
+    if kv_head_stride(v) != hs:
+        raise ValueError("k and v chunks must have the same head stride")
+    n_kv = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq,
+                                      n_kv, D, hs, scale, _dt(out.dtype),
+                                      _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_chunk_fwd")
+    return out, lse
+
+
+def attn_lse_merge(partials, lses, out=None, lse=None, out_dtype=torch.float32, stream=None):
+    """Merge p partials [p, B, H, N, D] (fp32 or bf16) with lses fp32 [p, B, H, N]."""
+    if not partials.is_cuda or partials.dim() != 5 or not partials.is_contiguous():
+        raise ValueError("partials must be a contiguous CUDA tensor [p, B, H, N, D]")
+    if lses.dtype != torch.float32 or tuple(lses.shape) != tuple(partials.shape[:4]) \
+            or not lses.is_contiguous():
+        raise ValueError("lses must be contiguous fp32 [p, B, H, N]")
+    p, B, H, N, D = partials.shape
+    if out is None:
+        out = torch.empty((B, H, N, D), device=partials.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, N), device=partials.device, dtype=torch.float32)
+    with torch.cuda.device(partials.device):
+        st = lib().dit_attn_lse_merge(_ptr(partials), _ptr(lses), p, _ptr(out), _ptr(lse), B, H, N,
+                                      D, _dt(partials.dtype), _dt(out.dtype),
+                                      _stream(partials.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_lse_merge")
+    return out, lse
+
+
+def check(device=None, stream=None):
+    """Synchronise and raise DitError if a kernel reported a timed-out wait."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = lib().dit_attn_check(_stream(dev, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_check")
+
+
+def inject_stall(enable: bool, wait_limit_cycles: int = 0):
+    """TEST ONLY: make later attention launches time out on their first K/V wait (see header)."""
+    lib().dit_test_inject_stall(1 if enable else 0, int(wait_limit_cycles))
+
+
+def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,
+                    partial_dtype=torch.float32, partials=None, lses=None, stream=None):
+    """Ring decomposition on one GPU: one dit_attn_chunk_fwd per KV chunk (virtual rank), then
+    one dit_attn_lse_merge.  `chunks` lists the chunk lengths (sum = N_kv)."""
+    B, H, Nq, D = q.shape
+    if sum(chunks) != k.shape[2]:
+        raise ValueError("chunk lengths must sum to the number of keys")
+    p = len(chunks)
+    if partials is None:
+        partials = torch.empty((p, B, H, Nq, D), device=q.device, dtype=partial_dtype)
+    if lses is None:
+        lses = torch.empty((p, B, H, Nq), device=q.device, dtype=torch.float32)
+    s = 0
+    for c, n in enumerate(chunks):
+        attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=partials[c], lse=lses[c],
+                       scale=scale, stream=stream)
+        s += n
+    return attn_lse_merge(partials, lses, out_dtype=out_dtype, stream=stream)
+
+
+def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
+              partial_dtype=torch.float32, device=None):
+    """User-level call.  Accepts CUDA tensors, or CPU tensors (ideally pinned) that are copied to
+    the device and whose results are copied back.  chunks=None runs the fused pass; a list of
+    chunk lengths runs the p-chunk ring decomposition with the LSE merge."""
+    on_host = not q.is_cuda
+    if on_host:
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        q = q.to(dev, non_blocking=True)
+        k = k.to(dev, non_blocking=True)
+        v = v.to(dev, non_blocking=True)
+    if chunks is None:
+        out, lse = attn_fwd(q, k, v, scale=scale, out_dtype=out_dtype)
+    else:
+        out, lse = chunk_attention(q, k, v, chunks, scale=scale, out_dtype=out_dtype,
+                                   partial_dtype=partial_dtype)
+    if on_host:
+        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream(q.device).synchronize()
+        return out_h, lse_h
+    return out, lse

@@ -1,0 +1,134 @@
+/*
+ * ditattn — non-causal DiT self-attention on GB300 (sm_103a), C ABI.
+ *
+ * The library computes O = softmax(scale * Q K^T) V per (batch, head) over
+ * long token sequences, either in one fused pass or as p KV chunks whose
+ * partial outputs and log-sum-exps are merged exactly as one Ring-attention
+ * hop merges them.  On one GPU the p chunks are virtual ranks: a "hop" is a
+ * pointer to the next chunk, with no communication.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are plain device pointers, contiguous row-major [B, H, N, D]
+ *    ("BHND"), except where a head stride is passed explicitly.  Q, K, V are
+ *    bf16 (IEEE binary16-brain, 2 bytes).  LSE buffers are fp32 [B, H, N].
+ *  - lse is the NATURAL log of sum_j exp(scale * q_i . k_j) over the keys the
+ *    call covers (the kernels work in base 2 internally and convert).
+ *  - The caller owns every buffer.  The library allocates no device memory;
+ *    it keeps only a cache of host-side TMA-descriptor encoders and one
+ *    device status word.
+ *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
+ *    errors are returned before anything is launched.  A launch failure
+ *    returns DIT_ERR_CUDA.  Device-side timeouts (a bounded wait that
+ *    expired) are recorded in the status word and reported by
+ *    dit_attn_check(), which synchronises the stream.
+ *  - Validation (before launch): B, H, N, n_kv, p >= 1; D in {64, 128} (else
+ *    DIT_ERR_UNSUPPORTED); pointers non-null; q, k, v, out, partials 16-byte
+ *    aligned; lse buffers 4-byte aligned; scale finite and > 0; outputs must
+ *    not overlap inputs; sizes must fit the kernels' 32-bit tile coordinates
+ *    (N < 2^31, B*H < 2^31).
+ */
+#ifndef DITATTN_H
+#define DITATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DIT_OK = 0,
+  DIT_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment, aliasing or scale */
+  DIT_ERR_UNSUPPORTED = 2,  /* valid request the kernels do not implement (e.g. D = 96) */
+  DIT_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  DIT_ERR_TIMEOUT = 4       /* a kernel's bounded wait expired (reported by dit_attn_check) */
+} dit_status;
+
+typedef enum { DIT_F32 = 0, DIT_BF16 = 1 } dit_dtype;
+
+/* Opaque CUDA stream (cudaStream_t / CUstream). */
+typedef void* dit_stream;
+
+/*
+ * Fused attention over all N keys.
+ * Defines: per head, s_ij = scale * q_i . k_j; o_i = sum_j softmax_j(s_ij) v_j;
+ * every query sees every key (non-causal).  Pages: MindIE-SD parallelism docs,
+ * "Ring Sequence Parallel" usage example (local attention = softmax of the
+ * scaled scores times V); arganzheng.life multi-GPU diffusion parallelism,
+ * section 4.1 Ulysses (full attention per head over all N tokens).
+ *   q, k, v : device bf16 [B, H, N, D], contiguous, 16-byte aligned (read only)
+ *   out     : device [B, H, N, D] of out_dtype (written)
+ *   lse     : device fp32 [B, H, N] (written)
+ *   scale   : score scale, usually 1/sqrt(D)
+ */
+dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int H, int N, int D, float scale, dit_dtype out_dtype,
+                        dit_stream stream);
+
+/*
+ * Attention of all N_q queries against ONE KV chunk: keys/values rows
+ * [0, n_kv) starting at k, v (pass pointers already offset to the chunk's
+ * first row).  This is one round of Ring attention: round i of rank r uses
+ * the K/V block of rank (r + i) mod p, and after p rounds every query has
+ * seen every key (arganzheng.life, section 4.2 Ring).
+ *   q              : device bf16 [B, H, N_q, D], contiguous
+ *   k, v           : device bf16; head (b*H + h) starts kv_head_stride
+ *                    elements after the previous one, rows are D elements
+ *                    apart.  N*D for a view into full [B,H,N,D] tensors,
+ *                    n_kv*D for a packed chunk buffer as a ring hop would
+ *                    receive it.  kv_head_stride must be >= n_kv*D and a
+ *                    multiple of 8 (16-byte TMA stride).
+ *   out_partial    : device [B, H, N_q, D] of partial_dtype: the softmax-
+ *                    normalised output over this chunk's keys
+ *   lse_partial    : device fp32 [B, H, N_q]: natural log-sum-exp over this chunk
+ */
+dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out_partial,
+                              float* lse_partial, int B, int H, int N_q, int n_kv, int D,
+                              long long kv_head_stride, float scale, dit_dtype partial_dtype,
+                              dit_stream stream);
+
+/*
+ * Exact merge of p chunk partials (O_c, lse_c) of the same queries:
+ *   M = max_c lse_c;  lse = M + ln sum_c exp(lse_c - M);  O = sum_c exp(lse_c - lse) O_c
+ * which is what the Ring section's online-softmax accumulation over the p
+ * rounds computes (arganzheng.life, section 4.2 Ring).  A chunk whose lse is
+ * -inf contributes nothing; a row whose lse_c are all -inf gets O = 0 and
+ * lse = -inf.
+ *   partials : device [p, B, H, N, D] of partial_dtype (chunk c at c*B*H*N*D)
+ *   lses     : device fp32 [p, B, H, N]
+ *   out      : device [B, H, N, D] of out_dtype;  lse: device fp32 [B, H, N]
+ */
+dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,
+                              float* lse, int B, int H, int N, int D, dit_dtype partial_dtype,
+                              dit_dtype out_dtype, dit_stream stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device status
+ * word.  Returns DIT_ERR_TIMEOUT if any kernel since the last check gave up
+ * on a bounded wait, DIT_ERR_CUDA if the synchronisation failed, else DIT_OK.
+ */
+dit_status dit_attn_check(dit_stream stream);
+
+/*
+ * TEST ONLY: failure injection for the timeout path.  While `enable` is
+ * non-zero, attention launches from this process load Q but never issue the
+ * K/V copies, so the MMA warp's bounded wait on the first K tile expires
+ * after `wait_limit_cycles` SM clocks (<= 0 keeps the default of about two
+ * seconds); the kernel then records DIT_ERR_TIMEOUT in the status word and
+ * exits cleanly, and dit_attn_check() reports it.  Nothing faults or hangs.
+ * Call with enable = 0 to restore normal operation.  Not thread-safe with
+ * concurrent launches from other host threads.
+ */
+void dit_test_inject_stall(int enable, long long wait_limit_cycles);
+
+/* Static, human-readable name of a status code. */
+const char* dit_status_string(dit_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DITATTN_H */

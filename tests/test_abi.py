@@ -1,0 +1,131 @@
+"""C-ABI boundary checks that need no GPU: the library builds, loads and exports
+every entry point include/ditattn.h declares, and argument validation rejects
+bad calls with the documented status before any CUDA call is made."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+from diffusion_transformer_long_gb300 import build as dbuild
+from diffusion_transformer_long_gb300 import ditattn as da
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ditattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build()
+    return da.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(dit_\w+)\s*\(", text, flags=re.M))
+
+
+def test_header_matches_binding():
+    assert declared_functions() == set(da.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", da.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_version_and_status_strings(lib):
+    assert lib.dit_version() == 100
+    assert da.status_string(da.DIT_OK) == "ok"
+    assert da.status_string(da.DIT_ERR_TIMEOUT) == "device wait timed out"
+    assert da.status_string(99) == "unknown status"
+
+
+# Fake, well-separated, 256-byte-aligned "device" addresses: validation never dereferences them.
+Q, K, V, OUT, LSE = (ctypes.c_void_p(a) for a in (1 << 40, 2 << 40, 3 << 40, 4 << 40, 5 << 40))
+
+
+def fwd(lib, q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, scale=0.088, dt=0):
+    return lib.dit_attn_fwd(q, k, v, out, lse, B, H, N, D, scale, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), da.DIT_ERR_INVALID_ARG), (dict(H=-1), da.DIT_ERR_INVALID_ARG),
+    (dict(N=0), da.DIT_ERR_INVALID_ARG), (dict(D=0), da.DIT_ERR_INVALID_ARG),
+    (dict(D=96), da.DIT_ERR_UNSUPPORTED), (dict(D=256), da.DIT_ERR_UNSUPPORTED),
+    (dict(q=None), da.DIT_ERR_INVALID_ARG), (dict(lse=None), da.DIT_ERR_INVALID_ARG),
+    (dict(k=ctypes.c_void_p((2 << 40) + 8)), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((4 << 40) + 4)), da.DIT_ERR_INVALID_ARG),
+    (dict(lse=ctypes.c_void_p((5 << 40) + 2)), da.DIT_ERR_INVALID_ARG),
+    (dict(scale=0.0), da.DIT_ERR_INVALID_ARG), (dict(scale=-1.0), da.DIT_ERR_INVALID_ARG),
+    (dict(scale=math.inf), da.DIT_ERR_INVALID_ARG), (dict(scale=math.nan), da.DIT_ERR_INVALID_ARG),
+    (dict(dt=7), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((1 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),   # out inside q
+    (dict(lse=ctypes.c_void_p((4 << 40) + 1024)), da.DIT_ERR_INVALID_ARG),   # lse inside out
+    (dict(B=1 << 16, H=1 << 16), da.DIT_ERR_INVALID_ARG),                    # B*H overflows int
+])
+def test_fwd_validation(lib, kw, status):
+    assert fwd(lib, **kw) == status
+
+
+def chunk(lib, n_kv=100, hs=256 * 128, D=128, **kw):
+    args = dict(q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, scale=0.088, dt=0)
+    args.update(kw)
+    return lib.dit_attn_chunk_fwd(args["q"], args["k"], args["v"], args["out"], args["lse"],
+                                  args["B"], args["H"], args["N"], n_kv, D, hs, args["scale"],
+                                  args["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_kv=0), da.DIT_ERR_INVALID_ARG),
+    (dict(n_kv=300, hs=256 * 128), da.DIT_ERR_INVALID_ARG),   # stride shorter than the chunk
+    (dict(hs=256 * 128 + 4), da.DIT_ERR_INVALID_ARG),         # stride not 16-byte aligned
+    (dict(hs=1 << 39), da.DIT_ERR_INVALID_ARG),
+    (dict(D=80), da.DIT_ERR_UNSUPPORTED),
+    (dict(k=ctypes.c_void_p((2 << 40) + 2)), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((2 << 40) + 64)), da.DIT_ERR_INVALID_ARG),     # out inside k
+])
+def test_chunk_validation(lib, kw, status):
+    assert chunk(lib, **kw) == status
+
+
+def merge(lib, p=4, parts=Q, lses=K, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, pdt=0, odt=0):
+    return lib.dit_attn_lse_merge(parts, lses, p, out, lse, B, H, N, D, pdt, odt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(p=0), da.DIT_ERR_INVALID_ARG), (dict(N=0), da.DIT_ERR_INVALID_ARG),
+    (dict(D=32), da.DIT_ERR_UNSUPPORTED), (dict(parts=None), da.DIT_ERR_INVALID_ARG),
+    (dict(parts=ctypes.c_void_p((1 << 40) + 8)), da.DIT_ERR_INVALID_ARG),
+    (dict(lses=ctypes.c_void_p((2 << 40) + 1)), da.DIT_ERR_INVALID_ARG),
+    (dict(pdt=3), da.DIT_ERR_INVALID_ARG), (dict(odt=-1), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((1 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),   # out inside partials
+    (dict(lse=ctypes.c_void_p((2 << 40) + 16)), da.DIT_ERR_INVALID_ARG),     # lse inside lses
+])
+def test_merge_validation(lib, kw, status):
+    assert merge(lib, **kw) == status
+
+
+def test_binding_rejects_host_tensors_and_bad_dtypes(lib):
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        da.attn_fwd(x, x, x)
+    with pytest.raises(TypeError):
+        da._dt(torch.float16)
+
+
+def test_kv_head_stride_of_views():
+    full = torch.zeros(2, 3, 40, 64)
+    assert da.kv_head_stride(full[:, :, 5:17]) == 40 * 64
+    assert da.kv_head_stride(torch.zeros(1, 1, 9, 64)) == 9 * 64
+    assert da.kv_head_stride(torch.zeros(4, 1, 9, 64)[:, :, 2:5]) == 9 * 64
+    with pytest.raises(ValueError):
+        da.kv_head_stride(full.transpose(2, 3))

@@ -1,0 +1,338 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (from the arithmetic: bf16 inputs, fp32 accumulation, bf16 P for
+the second GEMM): output max-abs <= 1e-2, mean-abs <= 1e-3 and LSE abs <= 1e-3
+for fp32 outputs.  A bf16 output is additionally allowed its own rounding: one
+bf16 ulp of the oracle value where that exceeds 1e-2.
+
+Small and FLUX-sized workloads are compared in full; Wan-sized ones on a
+seeded sample of query rows (all heads x 128 rows incl. the first/last 16),
+each sampled row exact in the oracle because rows are independent.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from diffusion_transformer_long_gb300 import ditattn as da
+from diffusion_transformer_long_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 1e-3
+DEV = torch.device("cuda:0")
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    a = np.abs(x).astype(np.float64)
+    e = np.floor(np.log2(np.maximum(a, 1e-30)))
+    return np.power(2.0, e - 7)
+
+
+def assert_parity(o, lse, o_ref, lse_ref, what, bf16_out=False):
+    o = o.detach().double().cpu().numpy()
+    lse = lse.detach().double().cpu().numpy()
+    err = np.abs(o - o_ref)
+    if bf16_out:
+        bound = np.maximum(MAX_ABS, bf16_ulp(o_ref))
+        assert (err <= bound).all(), f"{what}: bf16 out error {float((err - bound).max())} over bound"
+    else:
+        assert err.max() <= MAX_ABS, f"{what}: max-abs {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
+    lerr = np.abs(lse - lse_ref).max()
+    assert lerr <= LSE_ABS, f"{what}: lse {lerr:.3e}"
+    return float(err.max()), float(err.mean()), float(lerr)
+
+
+def to_dev(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def pick(o, lse, rows):
+    if rows is None:
+        return o, lse
+    idx = torch.as_tensor(rows, device=o.device)
+    return o.index_select(2, idx), lse.index_select(2, idx)
+
+
+# ----------------------------------------------------------------- workloads
+WORKLOAD_ROWS = {"tiny": None, "flux": None, "wan22": 128, "wan21": 128, "cfg": 512}
+
+
+@pytest.fixture(scope="module", params=list(synth.WORKLOADS))
+def workload(request):
+    w = synth.WORKLOADS[request.param]
+    q, k, v = synth.make_qkv(w)
+    nrows = WORKLOAD_ROWS[w.name]
+    rows = None if nrows is None else synth.sample_rows(w.N, nrows, seed=w.seed)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, rows=rows)
+    qd, kd, vd = to_dev(q, k, v)
+    del q, k, v
+    yield w, qd, kd, vd, rows, o_ref, lse_ref
+    del qd, kd, vd
+    torch.cuda.empty_cache()
+
+
+def test_fused_fp32(workload):
+    w, q, k, v, rows, o_ref, lse_ref = workload
+    o, lse = da.attn_fwd(q, k, v, scale=w.scale)
+    da.check()
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} fused fp32")
+
+
+def test_fused_bf16_out(workload):
+    w, q, k, v, rows, o_ref, lse_ref = workload
+    o, lse = da.attn_fwd(q, k, v, scale=w.scale, out_dtype=torch.bfloat16)
+    da.check()
+    assert o.dtype == torch.bfloat16
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} fused bf16", bf16_out=True)
+
+
+def test_chunk_merge_fp32_partials(workload):
+    w, q, k, v, rows, o_ref, lse_ref = workload
+    o, lse = da.chunk_attention(q, k, v, w.chunks, scale=w.scale)
+    da.check()
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} p={w.p} chunk+merge")
+    if w.alt_chunks:
+        o, lse = da.chunk_attention(q, k, v, w.alt_chunks, scale=w.scale)
+        da.check()
+        assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} uneven chunk+merge")
+
+
+def test_chunk_merge_bf16_partials(workload):
+    w, q, k, v, rows, o_ref, lse_ref = workload
+    o, lse = da.chunk_attention(q, k, v, w.chunks, scale=w.scale, partial_dtype=torch.bfloat16)
+    da.check()
+    # bf16 partials carry one bf16 rounding of each O_c: allow one ulp of the result
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} bf16 partials", bf16_out=True)
+
+
+def test_chunk_partials_match_oracle_chunks(workload):
+    """Each virtual rank's partial (O_c, lse_c) against the oracle over that chunk alone."""
+    w, q, k, v, rows, _, _ = workload
+    if w.name not in ("tiny", "wan22"):
+        pytest.skip("per-chunk check on two workloads")
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    for c, (s, n) in enumerate(zip(synth.chunk_starts(w.chunks), w.chunks)):
+        if c not in (0, len(w.chunks) - 1):
+            continue
+        o, lse = da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], scale=w.scale)
+        da.check()
+        o_ref, lse_ref = oracle.attention(qc, kc, vc, w.scale, kv_start=s, kv_len=n, rows=rows)
+        assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} chunk {c}")
+
+
+# ----------------------------------------------------------------- edge cases
+def rand_qkv(B, H, N, D, seed, nk=None, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    nk = N if nk is None else nk
+    q = (torch.randn(B, H, N, D, generator=g) * scale).to(torch.bfloat16)
+    k = (torch.randn(B, H, nk, D, generator=g) * scale).to(torch.bfloat16)
+    v = torch.randn(B, H, nk, D, generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("B,H,N,D", [
+    (1, 1, 1, 64), (1, 1, 1, 128), (1, 1, 7, 128), (1, 2, 129, 64), (2, 1, 200, 128),
+    (1, 1, 255, 128), (1, 3, 257, 64), (1, 1, 300, 128), (2, 3, 384, 128), (1, 1, 513, 64),
+    (1, 2, 1000, 128)])
+def test_ragged_shapes_full(B, H, N, D):
+    q, k, v = rand_qkv(B, H, N, D, seed=N + D)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = da.attn_fwd(qd, kd, vd, scale=scale)
+    da.check()
+    assert_parity(o, lse, o_ref, lse_ref, f"fused {B}x{H}x{N}x{D}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_ragged_chunks_views_and_packed(D):
+    N, chunks = 700, (1, 127, 128, 129, 315)
+    q, k, v = rand_qkv(2, 2, N, D, seed=D, scale=1.5)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = da.chunk_attention(qd, kd, vd, chunks, scale=scale)
+    da.check()
+    assert_parity(o, lse, o_ref, lse_ref, f"ragged chunks D={D}")
+    # a packed chunk buffer, as a ring hop would receive it (head stride n_kv*D)
+    s = 1 + 127
+    kp = kd[:, :, s:s + 128].contiguous()
+    vp = vd[:, :, s:s + 128].contiguous()
+    op, lp = da.attn_chunk_fwd(qd, kp, vp, scale=scale)
+    ov, lv = da.attn_chunk_fwd(qd, kd[:, :, s:s + 128], vd[:, :, s:s + 128], scale=scale)
+    da.check()
+    assert torch.equal(op, ov) and torch.equal(lp, lv)
+    oc, lc = oracle.attention(q, k, v, scale, kv_start=s, kv_len=128)
+    assert_parity(op, lp, oc, lc, "packed chunk")
+
+
+def test_query_and_key_counts_differ():
+    """N_q != n_kv (one chunk shorter than the queries), e.g. text K/V of 512 tokens."""
+    q, _, _ = rand_qkv(1, 2, 1300, 128, seed=5)
+    _, k, v = rand_qkv(1, 2, 512, 128, seed=6)
+    scale = 1 / math.sqrt(128)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    o, lse = da.attn_chunk_fwd(qd, kd, vd, scale=scale)
+    da.check()
+    assert_parity(o, lse, o_ref, lse_ref, "N_q=1300, n_kv=512")
+
+
+# ----------------------------------------------------------------- closed forms / invariants
+@pytest.fixture(scope="module")
+def flux_inputs():
+    w = synth.WORKLOADS["flux"]
+    q, k, v = synth.make_qkv(w)
+    return w, *to_dev(q, k, v)
+
+
+def test_q_zero_gives_mean_of_v(flux_inputs):
+    w, q, k, v = flux_inputs
+    o, lse = da.attn_fwd(torch.zeros_like(q), k, v, scale=w.scale)
+    da.check()
+    mean_v = v.double().mean(dim=2, keepdim=True).expand_as(o)
+    assert (o.double() - mean_v).abs().max().item() <= 1e-3
+    assert (lse.double() - math.log(w.N)).abs().max().item() <= 1e-4
+
+
+def test_v_ones_gives_ones(flux_inputs):
+    w, q, k, v = flux_inputs
+    o, _ = da.attn_fwd(q, k, torch.ones_like(v), scale=w.scale)
+    o2, _ = da.chunk_attention(q, k, torch.ones_like(v), w.chunks, scale=w.scale)
+    da.check()
+    assert (o - 1).abs().max().item() <= 2e-3
+    assert (o2 - 1).abs().max().item() <= 2e-3
+
+
+def test_kv_permutation_invariance(flux_inputs):
+    w, q, k, v = flux_inputs
+    perm = torch.randperm(w.N, generator=torch.Generator().manual_seed(9)).to(DEV)
+    o1, l1 = da.attn_fwd(q, k, v, scale=w.scale)
+    o2, l2 = da.attn_fwd(q, k[:, :, perm].contiguous(), v[:, :, perm].contiguous(), scale=w.scale)
+    da.check()
+    d = (o1 - o2).abs()
+    assert d.max().item() <= 2e-3 and d.mean().item() <= 1e-4
+    assert (l1 - l2).abs().max().item() <= 1e-4
+
+
+def test_fused_equals_chunk_merge(flux_inputs):
+    w, q, k, v = flux_inputs
+    o1, l1 = da.attn_fwd(q, k, v, scale=w.scale)
+    for p in (1, 2, 3, 7):
+        o2, l2 = da.chunk_attention(q, k, v, synth.even_chunks(w.N, p), scale=w.scale)
+        da.check()
+        d = (o1 - o2).abs()
+        assert d.max().item() <= 2e-3 and d.mean().item() <= 1e-4, p
+        assert (l1 - l2).abs().max().item() <= 1e-4, p
+
+
+def test_heads_independent(flux_inputs):
+    w, q, k, v = flux_inputs
+    o, lse = da.attn_fwd(q, k, v, scale=w.scale)
+    h = 5
+    o1, l1 = da.attn_fwd(q[:, h:h + 1].contiguous(), k[:, h:h + 1].contiguous(),
+                         v[:, h:h + 1].contiguous(), scale=w.scale)
+    da.check()
+    assert torch.equal(o1[:, 0], o[:, h]) and torch.equal(l1[:, 0], lse[:, h])
+
+
+# ----------------------------------------------------------------- merge kernel alone
+@pytest.mark.parametrize("pdt,odt", [(torch.float32, torch.float32), (torch.bfloat16, torch.float32),
+                                     (torch.float32, torch.bfloat16), (torch.bfloat16, torch.bfloat16)])
+@pytest.mark.parametrize("p,D", [(1, 128), (3, 64), (8, 128), (13, 128)])
+def test_merge_kernel_vs_oracle(p, D, pdt, odt):
+    g = torch.Generator().manual_seed(p * 100 + D)
+    B, H, N = 2, 3, 77
+    parts = torch.randn(p, B, H, N, D, generator=g).to(pdt)
+    lses = (torch.randn(p, B, H, N, generator=g) * 6).float()
+    if p > 1:
+        lses[0, 0, 0, :5] = -math.inf  # a chunk that saw nothing contributes nothing
+    o_ref, l_ref = oracle.lse_merge(parts.double().numpy(), lses.double().numpy())
+    o, l = da.attn_lse_merge(parts.to(DEV), lses.to(DEV), out_dtype=odt)
+    da.check()
+    tol = 1e-5 if odt == torch.float32 else None
+    od = o.double().cpu().numpy()
+    if tol is not None:
+        assert np.abs(od - o_ref).max() <= 1e-5 * max(1.0, np.abs(o_ref).max())
+    else:
+        assert (np.abs(od - o_ref) <= bf16_ulp(o_ref) * 0.5 + 1e-5).all()
+    assert np.abs(l.double().cpu().numpy() - l_ref).max() <= 1e-5
+
+
+def test_merge_all_minus_inf_row():
+    parts = torch.randn(3, 1, 1, 4, 64, device=DEV)
+    lses = torch.full((3, 1, 1, 4), -math.inf, device=DEV)
+    o, l = da.attn_lse_merge(parts, lses)
+    da.check()
+    assert (o == 0).all() and torch.isneginf(l).all()
+
+
+# ----------------------------------------------------------------- buffers and failures
+CANARY = -1.2345e30
+
+
+def test_canaries_untouched():
+    """Outputs written through slices of larger buffers: nothing outside is touched."""
+    B, H, N, D, pad = 1, 2, 333, 128, 1024
+    q, k, v = to_dev(*rand_qkv(B, H, N, D, seed=77))
+    n_out = B * H * N * D
+    big = torch.full((n_out + 2 * pad,), CANARY, device=DEV)
+    big_l = torch.full((B * H * N + 2 * pad,), CANARY, device=DEV)
+    out = big[pad:pad + n_out].view(B, H, N, D)
+    lse = big_l[pad:pad + B * H * N].view(B, H, N)
+    da.attn_fwd(q, k, v, out=out, lse=lse)
+    parts = torch.full((3 * n_out + 2 * pad,), CANARY, device=DEV)
+    lses = torch.full((3 * B * H * N + 2 * pad,), CANARY, device=DEV)
+    P = parts[pad:pad + 3 * n_out].view(3, B, H, N, D)
+    L = lses[pad:pad + 3 * B * H * N].view(3, B, H, N)
+    s = 0
+    for c, n in enumerate((100, 133, 100)):
+        da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=P[c], lse=L[c])
+        s += n
+    mo = torch.full((n_out + 2 * pad,), CANARY, device=DEV)
+    ml = torch.full((B * H * N + 2 * pad,), CANARY, device=DEV)
+    da.attn_lse_merge(P, L, out=mo[pad:pad + n_out].view(B, H, N, D),
+                      lse=ml[pad:pad + B * H * N].view(B, H, N))
+    da.check()
+    for buf, n in ((big, n_out), (big_l, B * H * N), (parts, 3 * n_out), (lses, 3 * B * H * N),
+                   (mo, n_out), (ml, B * H * N)):
+        assert (buf[:pad] == CANARY).all() and (buf[pad + n:] == CANARY).all()
+        assert torch.isfinite(buf[pad:pad + n]).all()
+    assert torch.allclose(mo[pad:pad + n_out].view(B, H, N, D), out, atol=2e-3)
+
+
+def test_timeout_is_reported_and_context_survives():
+    """Failure injection: K/V copies are never issued, the bounded wait (~10 ms) expires, the
+    kernel exits cleanly and dit_attn_check reports DIT_ERR_TIMEOUT; later calls work."""
+    q, k, v = to_dev(*rand_qkv(1, 1, 256, 128, seed=3))
+    da.check()
+    da.inject_stall(True, 20_000_000)
+    try:
+        da.attn_fwd(q, k, v)
+        with pytest.raises(da.DitError) as e:
+            da.check()
+        assert e.value.status == da.DIT_ERR_TIMEOUT
+    finally:
+        da.inject_stall(False)
+    da.check()  # status was cleared
+    o, lse = da.attn_fwd(q, k, v)
+    da.check()
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), 1 / math.sqrt(128))
+    assert_parity(o, lse, o_ref, lse_ref, "after timeout")
+
+
+def test_device_validation_errors():
+    q, k, v = to_dev(*rand_qkv(1, 1, 64, 128, seed=1))
+    L = da.lib()
+    out = torch.empty(1, 1, 64, 128, device=DEV)
+    lse = torch.empty(1, 1, 64, device=DEV)
+    st = L.dit_attn_fwd(da._ptr(q), da._ptr(k), da._ptr(v), da._ptr(out), da._ptr(lse), 1, 1, 64,
+                        96, 0.1, 0, None)
+    assert st == da.DIT_ERR_UNSUPPORTED
+    st = L.dit_attn_fwd(da._ptr(q), da._ptr(k), da._ptr(v), da._ptr(q), da._ptr(lse), 1, 1, 64,
+                        128, 0.1, 0, None)
+    assert st == da.DIT_ERR_INVALID_ARG  # output aliases an input
