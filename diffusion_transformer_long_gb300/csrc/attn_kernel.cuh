@@ -281,9 +281,19 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       for (int i = 0; i < kBlockN; ++i)
         if (i >= valid) s[i] = -INFINITY;
     }
-    float mx = s[0];
+    // Tile row max: 8 independent 3-input max chains, then a short tree.
+    float mx;
+    {
+      float a[8];
 #pragma unroll
-    for (int i = 1; i < kBlockN; ++i) mx = fmaxf(mx, s[i]);
+      for (int g = 0; g < 8; ++g) {
+        a[g] = ptx::fmax3(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
+#pragma unroll
+        for (int i = 3; i < 15; i += 2) a[g] = ptx::fmax3(a[g], s[16 * g + i], s[16 * g + i + 1]);
+        a[g] = fmaxf(a[g], s[16 * g + 15]);
+      }
+      mx = ptx::fmax3(ptx::fmax3(a[0], a[1], a[2]), ptx::fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+    }
     const float m_tile = mx * c;
     const bool raise = m_tile > m + kRescaleLog2;  // always true on the first tile
     float alpha = 1.f;
@@ -307,29 +317,47 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       ptx::tmem_wait_st();
     }
 
-    const float neg_m = -m;
-    float rs = 0.f;
+    // P = 2^(c*s - m), two elements per packed FMA.
+    const uint64_t c2 = ptx::f2pack(c, c);
+    const uint64_t nm2 = ptx::f2pack(-m, -m);
 #pragma unroll
-    for (int i = 0; i < kBlockN; ++i) {
-      s[i] = ptx::ex2_approx(fmaf(s[i], c, neg_m));
-      rs += s[i];
+    for (int i = 0; i < kBlockN; i += 2) {
+      float x0, x1;
+      ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[i], s[i + 1]), c2, nm2), x0, x1);
+      s[i] = ptx::ex2_approx(x0);
+      s[i + 1] = ptx::ex2_approx(x1);
     }
-    l += rs;
 
-    // P row r -> two 128-byte-swizzled K-major regions (keys 0-63, 64-127).
+    // Pack P to bf16, store it (row r -> two 128-byte-swizzled K-major regions: keys 0-63,
+    // 64-127), and accumulate both row sums in 4 independent packed chains each.
+    uint64_t acc_l[4], acc_lp[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) acc_l[g] = acc_lp[g] = 0;
 #pragma unroll
     for (int ch = 0; ch < kBlockN / 8; ++ch) {
-      const uint32_t w0 = ptx::pack_bf16x2(s[8 * ch + 0], s[8 * ch + 1]);
-      const uint32_t w1 = ptx::pack_bf16x2(s[8 * ch + 2], s[8 * ch + 3]);
-      const uint32_t w2 = ptx::pack_bf16x2(s[8 * ch + 4], s[8 * ch + 5]);
-      const uint32_t w3 = ptx::pack_bf16x2(s[8 * ch + 6], s[8 * ch + 7]);
-      lp += (ptx::bf16lo(w0) + ptx::bf16hi(w0)) + (ptx::bf16lo(w1) + ptx::bf16hi(w1)) +
-            (ptx::bf16lo(w2) + ptx::bf16hi(w2)) + (ptx::bf16lo(w3) + ptx::bf16hi(w3));
+      uint32_t w[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const float p0 = s[8 * ch + 2 * g], p1 = s[8 * ch + 2 * g + 1];
+        w[g] = ptx::pack_bf16x2(p0, p1);
+        acc_l[g] = ptx::fadd2(acc_l[g], ptx::f2pack(p0, p1));
+        acc_lp[g] = ptx::fadd2(acc_lp[g], ptx::f2pack(ptx::bf16lo(w[g]), ptx::bf16hi(w[g])));
+      }
       const uint32_t addr =
           sP + (ch / 8) * L::kRegion + r * 128 + ((((ch % 8) ^ (r & 7))) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0), "r"(w1),
-                   "r"(w2), "r"(w3)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                   "r"(w[2]), "r"(w[3])
                    : "memory");
+    }
+    {
+      const uint64_t sl = ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
+      const uint64_t sp = ptx::fadd2(ptx::fadd2(acc_lp[0], acc_lp[1]),
+                                     ptx::fadd2(acc_lp[2], acc_lp[3]));
+      float a0, a1, b0, b1;
+      ptx::f2unpack(sl, a0, a1);
+      ptx::f2unpack(sp, b0, b1);
+      l += a0 + a1;
+      lp += b0 + b1;
     }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
