@@ -10,26 +10,33 @@
 // the fused pass (n_kv = N) and one KV chunk of the ring decomposition (K/V
 // pointers offset to the chunk, n_kv = chunk length, explicit head stride).
 //
-// CTA organisation (320 threads, one CTA per SM):
+// CTA organisation (352 threads, one CTA per SM):
 //   warps 0-3  softmax for Q tile 0   (thread = query row = TMEM lane)
 //   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer (Q once, then K_j / V_j through a 3-slot ring)
-//   warp  9    TMEM allocator + single-thread tcgen05.mma issuer
+//   warp  8    TMA producer (Q once, then K/V tiles through a 3-slot ring)
+//   warp  9    TMEM allocator + single-thread issuer of S = Q K^T
+//   warp 10    single-thread issuer of O += P V
+// Two issuers keep the tensor pipe fed: its queue is about one instruction deep,
+// and a barrier wait stalls the waiting thread for longer than one MMA, so while
+// one issuer waits the other issues.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, fp32, lane = query row.
 // Shared memory: Q0, Q1, P0, P1 (bf16 probabilities, written by the softmax
 // warps in the 128-byte-swizzled K-major layout the MMA reads) and the K/V ring.
 //
-// Per KV tile j the MMA warp issues, in order,
-//   O0 += P0_j V_j ; S0 = Q0 K_{j+1}^T ; O1 += P1_j V_j ; S1 = Q1 K_{j+1}^T
-// so the tensor core works on one Q tile while the other tile's softmax runs.
-// A commit after S_t(j+1) also covers PV_t(j), so when softmax t sees S_t(j+1)
-// ready, O_t and P_t are free: one S, O and P buffer per Q tile suffice.
+// Pipeline.  A softmax warpgroup releases its S buffer (S_EMPTY) as soon as
+// the scores are in registers, so the MMA warp computes S_t(j+1) = Q_t K_{j+1}^T
+// while softmax t is still turning S_t(j) into probabilities; softmax t can
+// start tile j+1 the moment it has published P_t(j) (P_FULL).  O_t += P_t(j) V_j
+// is committed to its own barrier (PV_DONE), which softmax t waits on only
+// before it rescales O_t or overwrites the P_t buffer.  Per KV tile the S issuer
+// issues S0(j+1), S1(j+1) and the PV issuer PV0(j), PV1(j); the K/V ring is filled
+// in consumption order: K0, K1, V0, K2, V1, ...
 //
 // Online softmax (base 2, scale folded into log2e): the running max m is only
-// raised when a tile's max exceeds it by more than kRescaleLog2 (then O and l
-// are rescaled by 2^(m_old - m_new)); otherwise exponentials are taken against
-// the stale m, which bounds P by 2^kRescaleLog2.  The result is exact either
-// way: O / l and m + log2 l do not depend on which m was used.
+// raised when a tile's max exceeds it by more than kRescaleLog2 (then O and the
+// row sums are rescaled by 2^(m_old - m_new)); otherwise exponentials are taken
+// against the stale m, which bounds P by 2^kRescaleLog2.  The result is exact
+// either way: O / l and m + log2 l do not depend on which m was used.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,14 +44,40 @@
 
 #include "sm103_ptx.cuh"
 
+// Optional phase tracing (compile with -DDITATTN_TRACE): one CTA records SM-clock
+// timestamps of pipeline events for its first 64 KV tiles into
+// ditattn_trace_buf[event][tile].  Compiled out by default.
+#ifdef DITATTN_TRACE
+#ifndef DITATTN_TRACE_CTA
+#define DITATTN_TRACE_CTA 0
+#endif
+__device__ long long ditattn_trace_buf[32 * 64];
+#define DIT_TRACE(ev, j)                                                   \
+  do {                                                                      \
+    if (blockIdx.x == DITATTN_TRACE_CTA && (j) >= 0 && (j) < 64)            \
+      ditattn_trace_buf[(ev) * 64 + (j)] = clock64();                       \
+  } while (0)
+#else
+#define DIT_TRACE(ev, j) \
+  do {                   \
+  } while (0)
+#endif
+
 namespace ditattn {
+
+enum TraceEvent {
+  kTrProdEmpty = 0, kTrProdIssue, kTrMmaK, kTrMmaS0, kTrMmaS1, kTrMmaV, kTrMmaP0, kTrMmaPv0,
+  kTrMmaP1, kTrMmaPv1, kTrSmFull0, kTrSmLd0, kTrSmMax0, kTrSmExp0, kTrSmArrive0,
+  kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1
+};
 
 constexpr int kBlockM = 128;              // query rows per Q tile (two per CTA)
 constexpr int kBlockN = 128;              // keys per KV tile
 constexpr int kStages = 3;                // K/V ring slots
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;     // S = Q K^T issuer, owns the TMEM allocation
+constexpr int kPvWarp = 10;     // O += P V issuer
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
@@ -79,13 +112,16 @@ struct AttnSmem {
   static constexpr uint32_t kBars = kKV + kStages * kTile;
   // barrier indices
   static constexpr int bQFull = 0;
-  static constexpr int bKVFull = 1;                  // + slot
-  static constexpr int bKVEmpty = bKVFull + kStages; // + slot
-  static constexpr int bSFull = bKVEmpty + kStages;  // + tile
-  static constexpr int bPFull = bSFull + 2;          // + tile
-  static constexpr int bODone = bPFull + 2;
-  static constexpr int bDrain = bODone + 1;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bKFull = 1;                   // + slot: a K tile landed in the slot
+  static constexpr int bVFull = bKFull + kStages;    // + slot: a V tile landed in the slot
+  static constexpr int bKVEmpty = bVFull + kStages;  // + slot: the slot's tile was consumed
+  static constexpr int bSFull = bKVEmpty + kStages;  // + tile: S_t computed (MMA commit)
+  static constexpr int bSEmpty = bSFull + 2;         // + tile: S_t read into registers (128 arrivals)
+  static constexpr int bPFull = bSEmpty + 2;         // + tile: P_t written (128 arrivals)
+  static constexpr int bPVDone = bPFull + 2;         // + tile: O_t += P_t V done (MMA commit)
+  static constexpr int bDrainS = bPVDone + 2;        // abort drain, S issuer
+  static constexpr int bDrainPV = bDrainS + 1;       // abort drain, PV issuer
+  static constexpr int kNumBars = bDrainPV + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kUsed = kAbort + 4;
@@ -112,6 +148,14 @@ __device__ __forceinline__ void raise_abort(const AttnParams& p, volatile int* a
   atomicOr(p.status, kStatusTimeout);
 }
 
+// K/V ring items in consumption order: K_0, then per KV tile j: K_{j+1} (if any), V_j.
+// Item i goes to slot i % kStages.  K and V tiles landing in a slot complete different
+// barriers (K_FULL / V_FULL), so each MMA issuer observes the phases of only the
+// barriers it consumes, in order, and can never mistake an older fill for a newer one.
+__device__ __forceinline__ int v_item(int j, int n_tiles) {
+  return (j + 1 < n_tiles) ? 2 * j + 2 : 2 * j + 1;
+}
+
 template <int D>
 __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, int bh, int q_row0,
                                          int n_tiles, volatile int* abort_flag) {
@@ -129,27 +173,43 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
 
   if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
 
-  int last_it[kStages];
+  uint32_t kpar = 0, vpar = 0;  // bit s: parity of the next K_FULL[s] / V_FULL[s] phase
+  int last_bar[kStages];        // barrier and parity of the newest copy into each slot
+  uint32_t last_par[kStages];
 #pragma unroll
-  for (int s = 0; s < kStages; ++s) last_it[s] = -1;
-  bool ok = true;
-  for (int it = 0; it < 2 * n_tiles; ++it) {
+  for (int s = 0; s < kStages; ++s) {
+    last_bar[s] = -1;
+    last_par[s] = 0;
+  }
+  int it = 0;
+  auto load = [&](bool is_v, int tile) {
     const int s = it % kStages;
     const uint32_t ph = (it / kStages) & 1;
-    if (!wait_or_abort(bar(L::bKVEmpty + s), ph ^ 1, abort_flag, p.wait_limit)) {
-      ok = false;
-      break;
-    }
-    const CUtensorMap* tm = (it & 1) ? &p.tm_v : &p.tm_k;
-    const int j = it >> 1;
-    ptx::mbar_arrive_expect_tx(bar(L::bKVFull + s), L::kTile);
+    if (!wait_or_abort(bar(L::bKVEmpty + s), ph ^ 1, abort_flag, p.wait_limit)) return false;
+    DIT_TRACE(kTrProdEmpty, it);
+    const int fb = (is_v ? L::bVFull : L::bKFull) + s;
+    const uint32_t par = ((is_v ? vpar : kpar) >> s) & 1;
+    if (is_v) vpar ^= 1u << s; else kpar ^= 1u << s;
+    ptx::mbar_arrive_expect_tx(bar(fb), L::kTile);
+    const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
     for (int r = 0; r < kRegions; ++r)
-      ptx::tma_load_3d(sbase + L::kKV + s * L::kTile + r * L::kRegion, tm, bar(L::bKVFull + s),
-                       r * 64, j * kBlockN, bh);
+      ptx::tma_load_3d(sbase + L::kKV + s * L::kTile + r * L::kRegion, tm, bar(fb), r * 64,
+                       tile * kBlockN, bh);
+    DIT_TRACE(kTrProdIssue, it);
 #pragma unroll
     for (int q = 0; q < kStages; ++q)
-      if (q == s) last_it[q] = it;
+      if (q == s) {
+        last_bar[q] = fb;
+        last_par[q] = par;
+      }
+    ++it;
+    return true;
+  };
+  bool ok = load(false, 0);
+  for (int j = 0; ok && j < n_tiles; ++j) {
+    if (j + 1 < n_tiles && !(ok = load(false, j + 1))) break;
+    ok = load(true, j);
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -157,88 +217,168 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     ptx::mbar_wait(bar(L::bQFull), 0, p.wait_limit);
 #pragma unroll
     for (int s = 0; s < kStages; ++s)
-      if (last_it[s] >= 0)
-        ptx::mbar_wait(bar(L::bKVFull + s), (last_it[s] / kStages) & 1, p.wait_limit);
+      if (last_bar[s] >= 0) ptx::mbar_wait(bar(last_bar[s]), last_par[s], p.wait_limit);
   }
 }
 
+// Shared-memory matrix descriptors.  The high word (stride byte offset 1024,
+// version 1, 128-byte swizzle) is common to every operand; the low word holds the
+// start address and the leading byte offset.  Low words are precomputed per buffer
+// so that issuing one MMA costs one 32-bit add per operand.
 template <int D>
-__device__ __forceinline__ void mma_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
-                                           int n_tiles, volatile int* abort_flag) {
+struct Descs {
+  static constexpr uint32_t kHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+  uint32_t q[2], pp[2], k[kStages], v[kStages];
+  __device__ __forceinline__ static uint32_t lo(uint32_t addr, uint32_t lbo) {
+    return (addr >> 4) | ((lbo >> 4) << 16);
+  }
+  __device__ __forceinline__ static uint64_t full(uint32_t lo_word) {
+    return (static_cast<uint64_t>(kHi) << 32) | static_cast<uint64_t>(lo_word);
+  }
+  __device__ __forceinline__ explicit Descs(uint32_t sbase) {
+    using L = AttnSmem<D>;
+    q[0] = lo(sbase + L::kQ0, 16);
+    q[1] = lo(sbase + L::kQ1, 16);
+    pp[0] = lo(sbase + L::kP0, 16);
+    pp[1] = lo(sbase + L::kP1, 16);
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) {
+      k[s] = lo(sbase + L::kKV + s * L::kTile, 16);          // K-major K tile
+      v[s] = lo(sbase + L::kKV + s * L::kTile, L::kRegion);  // MN-major V tile
+    }
+  }
+  __device__ __forceinline__ static uint32_t pick(const uint32_t (&a)[kStages], int slot) {
+    uint32_t r = a[0];
+#pragma unroll
+    for (int s = 1; s < kStages; ++s)
+      if (slot == s) r = a[s];
+    return r;
+  }
+};
+
+// S_t = Q_t K^T for every KV tile (warp kMmaWarp, one thread).
+template <int D>
+__device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
+                                         int n_tiles, volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
-  constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kBlockM, D, false, true);
-  const uint32_t qs[2] = {sbase + L::kQ0, sbase + L::kQ1};
-  const uint32_t ps[2] = {sbase + L::kP0, sbase + L::kP1};
-
-  // S_t = Q_t K^T: K-major A and B, 16 keys' worth of D per instruction.
-  auto issue_s = [&](int t, int slot) {
-    const uint32_t kb = sbase + L::kKV + slot * L::kTile;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
+  const Descs<D> ds(sbase);
+  // K-major A and B, 16 of D's elements per instruction: the K-step advances 32 bytes
+  // inside a 128-byte swizzle column, then moves to the next column.
+  auto issue = [&](int t, int slot) {
+    const uint32_t kb = Descs<D>::pick(ds.k, slot);
+    const uint32_t qa = ds.q[t];
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k / 4) * L::kRegion + (k % 4) * 32;
-      ptx::mma_bf16_ss(tmem + t * kBlockN, ptx::sdesc_sw128(qs[t] + off, 16, 1024),
-                       ptx::sdesc_sw128(kb + off, 16, 1024), kIdescQK, k > 0 ? 1u : 0u);
+      const uint32_t off = ((k / 4) * L::kRegion + (k % 4) * 32) >> 4;
+      ptx::mma_bf16_ss(tmem + t * kBlockN, Descs<D>::full(qa + off), Descs<D>::full(kb + off),
+                       kIdesc, k > 0 ? 1u : 0u);
     }
   };
-  // O_t += P_t V: P K-major, V MN-major (D contiguous); 16 keys per instruction.
-  auto issue_pv = [&](int t, int slot, bool acc) {
-    const uint32_t vb = sbase + L::kKV + slot * L::kTile;
-#pragma unroll
-    for (int k = 0; k < kBlockN / 16; ++k) {
-      const uint32_t aoff = (k / 4) * L::kRegion + (k % 4) * 32;
-      ptx::mma_bf16_ss(tmem + 2 * kBlockN + t * D, ptx::sdesc_sw128(ps[t] + aoff, 16, 1024),
-                       ptx::sdesc_sw128(vb + k * 16 * 128, L::kRegion, 1024), kIdescPV,
-                       (acc || k > 0) ? 1u : 0u);
-    }
+  auto wait = [&](int b, uint32_t parity) {
+    return wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
   };
-  auto kv_wait = [&](int it) {
-    return wait_or_abort(bar(L::bKVFull + it % kStages), (it / kStages) & 1, abort_flag,
-                         p.wait_limit);
+  uint32_t kpar = 0;  // bit s: parity of the next K_FULL[s] phase
+  auto wait_k = [&](int s) {
+    const bool r = wait(L::bKFull + s, (kpar >> s) & 1);
+    kpar ^= 1u << s;
+    return r;
   };
 
-  bool ok = wait_or_abort(bar(L::bQFull), 0, abort_flag, p.wait_limit) && kv_wait(0);
+  bool ok = wait(L::bQFull, 0) && wait_k(0);
   if (ok) {
     ptx::tc_fence_after();
-    issue_s(0, 0);
+    issue(0, 0);
     ptx::mma_commit(bar(L::bSFull + 0));
-    issue_s(1, 0);
+    issue(1, 0);
     ptx::mma_commit(bar(L::bSFull + 1));
     ptx::mma_commit(bar(L::bKVEmpty + 0));
   }
-  for (int j = 0; ok && j < n_tiles; ++j) {
-    const int itV = 2 * j + 1, sV = itV % kStages;
-    const int itK = 2 * j + 2, sK = itK % kStages;
-    const bool more = j + 1 < n_tiles;
-    if (!(ok = kv_wait(itV))) break;
-    if (!(ok = wait_or_abort(bar(L::bPFull + 0), j & 1, abort_flag, p.wait_limit))) break;
+  for (int j = 0; ok && j + 1 < n_tiles; ++j) {
+    const int sK = (2 * j + 1) % kStages;  // ring item of K_{j+1}
+    if (!(ok = wait_k(sK))) break;
+    DIT_TRACE(kTrMmaK, j);
+    if (!(ok = wait(L::bSEmpty + 0, j & 1))) break;
     ptx::tc_fence_after();
-    issue_pv(0, sV, j > 0);
-    if (more) {
-      if (!(ok = kv_wait(itK))) break;
-      ptx::tc_fence_after();
-      issue_s(0, sK);
-      ptx::mma_commit(bar(L::bSFull + 0));
-    }
-    if (!(ok = wait_or_abort(bar(L::bPFull + 1), j & 1, abort_flag, p.wait_limit))) break;
+    issue(0, sK);
+    ptx::mma_commit(bar(L::bSFull + 0));
+    DIT_TRACE(kTrMmaS0, j);
+    if (!(ok = wait(L::bSEmpty + 1, j & 1))) break;
     ptx::tc_fence_after();
-    issue_pv(1, sV, j > 0);
-    ptx::mma_commit(bar(L::bKVEmpty + sV));
-    if (more) {
-      issue_s(1, sK);
-      ptx::mma_commit(bar(L::bSFull + 1));
-      ptx::mma_commit(bar(L::bKVEmpty + sK));
-    }
+    issue(1, sK);
+    ptx::mma_commit(bar(L::bSFull + 1));
+    ptx::mma_commit(bar(L::bKVEmpty + sK));
+    DIT_TRACE(kTrMmaS1, j);
   }
-  if (ok) {
-    ptx::mma_commit(bar(L::bODone));
-  } else {
+  if (!ok) {
     raise_abort(p, abort_flag);
     // No MMA may still be writing tensor memory when it is released.
-    ptx::mma_commit(bar(L::bDrain));
-    ptx::mbar_wait(bar(L::bDrain), 0, p.wait_limit);
+    ptx::mma_commit(bar(L::bDrainS));
+    ptx::mbar_wait(bar(L::bDrainS), 0, p.wait_limit);
   }
+}
+
+// O_t += P_t V_j for every KV tile (warp kPvWarp, one thread).
+template <int D>
+__device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
+                                          int n_tiles, volatile int* abort_flag) {
+  using L = AttnSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, D, false, true);
+  const Descs<D> ds(sbase);
+  // P K-major, V MN-major (D contiguous); 16 keys (2 KB of V) per instruction.
+  auto issue = [&](int t, int slot, bool acc) {
+    const uint32_t vb = Descs<D>::pick(ds.v, slot);
+    const uint32_t pa = ds.pp[t];
+#pragma unroll
+    for (int k = 0; k < kBlockN / 16; ++k) {
+      const uint32_t aoff = ((k / 4) * L::kRegion + (k % 4) * 32) >> 4;
+      ptx::mma_bf16_ss(tmem + 2 * kBlockN + t * D, Descs<D>::full(pa + aoff),
+                       Descs<D>::full(vb + k * 128), kIdesc, (acc || k > 0) ? 1u : 0u);
+    }
+  };
+  auto wait = [&](int b, uint32_t parity) {
+    return wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
+  };
+  uint32_t vpar = 0;  // bit s: parity of the next V_FULL[s] phase
+
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int sV = v_item(j, n_tiles) % kStages;
+    if (!(ok = wait(L::bPFull + 0, j & 1))) break;
+    DIT_TRACE(kTrMmaP0, j);
+    ok = wait(L::bVFull + sV, (vpar >> sV) & 1);
+    vpar ^= 1u << sV;
+    if (!ok) break;
+    DIT_TRACE(kTrMmaV, j);
+    ptx::tc_fence_after();
+    issue(0, sV, j > 0);
+    ptx::mma_commit(bar(L::bPVDone + 0));
+    DIT_TRACE(kTrMmaPv0, j);
+    if (!(ok = wait(L::bPFull + 1, j & 1))) break;
+    DIT_TRACE(kTrMmaP1, j);
+    ptx::tc_fence_after();
+    issue(1, sV, j > 0);
+    ptx::mma_commit(bar(L::bPVDone + 1));
+    ptx::mma_commit(bar(L::bKVEmpty + sV));
+    DIT_TRACE(kTrMmaPv1, j);
+  }
+  if (!ok) {
+    raise_abort(p, abort_flag);
+    ptx::mma_commit(bar(L::bDrainPV));
+    ptx::mbar_wait(bar(L::bDrainPV), 0, p.wait_limit);
+  }
+}
+
+// acc_lo += low bf16 of w, acc_hi += high bf16 of w (exact widening, fp32 add).
+__device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(w));
 }
 
 template <int D, bool kOutF32>
@@ -255,14 +395,19 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
   const uint32_t tO = tmem + 2 * kBlockN + t * D + lane_off;
   const uint32_t sP = sbase + (t ? L::kP1 : L::kP0);
   const float c = p.scale_log2;
+  // Warp-uniform bounded wait.
+  auto wait = [&](int b, uint32_t parity) {
+    const bool ok = wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
+    return __all_sync(0xffffffffu, ok);
+  };
 
   float m = -INFINITY;  // running max of scale*log2e*s (possibly stale by < 2^8)
   float l = 0.f;        // running sum of 2^(c*s - m), for the LSE
   float lp = 0.f;       // running sum of the bf16-rounded P the PV GEMM sees, for O
   bool ok = true;
   for (int j = 0; j < n_tiles; ++j) {
-    ok = wait_or_abort(bar(L::bSFull + t), j & 1, abort_flag, p.wait_limit);
-    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+    if (!(ok = wait(L::bSFull + t, j & 1))) break;
+    if (r == 0) DIT_TRACE(kTrSmFull0 + 5 * t, j);
     ptx::tc_fence_after();
 
     float s[kBlockN];
@@ -274,6 +419,10 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
     }
     ptx::tmem_wait_ld();
+    // S_t is in registers: the MMA warp may overwrite it with S_t(j+1).
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(bar(L::bSEmpty + t));
+    if (r == 0) DIT_TRACE(kTrSmLd0 + 5 * t, j);
 
     const int valid = p.n_kv - j * kBlockN;
     if (valid < kBlockN) {
@@ -294,6 +443,7 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       }
       mx = ptx::fmax3(ptx::fmax3(a[0], a[1], a[2]), ptx::fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
     }
+    if (r == 0) DIT_TRACE(kTrSmMax0 + 5 * t, j);
     const float m_tile = mx * c;
     const bool raise = m_tile > m + kRescaleLog2;  // always true on the first tile
     float alpha = 1.f;
@@ -303,8 +453,12 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
     }
     l *= alpha;
     lp *= alpha;
+    bool pv_prev_done = (j == 0);
     if (j > 0 && __any_sync(0xffffffffu, raise)) {
-      // PV_t(j-1) has completed (covered by the commit after S_t(j)); rescale O_t.
+      // O_t may only be touched once PV_t(j-1) has landed.
+      if (!(ok = wait(L::bPVDone + t, (j - 1) & 1))) break;
+      pv_prev_done = true;
+      ptx::tc_fence_after();
 #pragma unroll
       for (int cc = 0; cc < D / 16; ++cc) {
         uint32_t u[16];
@@ -327,12 +481,19 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       s[i] = ptx::ex2_approx(x0);
       s[i + 1] = ptx::ex2_approx(x1);
     }
+    if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, j);
+
+    // The P_t buffer is free once PV_t(j-1) has read it.
+    if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (j - 1) & 1))) break;
 
     // Pack P to bf16, store it (row r -> two 128-byte-swizzled K-major regions: keys 0-63,
-    // 64-127), and accumulate both row sums in 4 independent packed chains each.
-    uint64_t acc_l[4], acc_lp[4];
+    // 64-127), and accumulate both row sums in independent chains.
+    uint64_t acc_l[4];
+    float acc_lp[8];
 #pragma unroll
-    for (int g = 0; g < 4; ++g) acc_l[g] = acc_lp[g] = 0;
+    for (int g = 0; g < 4; ++g) acc_l[g] = 0;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) acc_lp[g] = 0.f;
 #pragma unroll
     for (int ch = 0; ch < kBlockN / 8; ++ch) {
       uint32_t w[4];
@@ -341,7 +502,7 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
         const float p0 = s[8 * ch + 2 * g], p1 = s[8 * ch + 2 * g + 1];
         w[g] = ptx::pack_bf16x2(p0, p1);
         acc_l[g] = ptx::fadd2(acc_l[g], ptx::f2pack(p0, p1));
-        acc_lp[g] = ptx::fadd2(acc_lp[g], ptx::f2pack(ptx::bf16lo(w[g]), ptx::bf16hi(w[g])));
+        add_bf16x2(acc_lp[2 * g], acc_lp[2 * g + 1], w[g]);
       }
       const uint32_t addr =
           sP + (ch / 8) * L::kRegion + r * 128 + ((((ch % 8) ^ (r & 7))) << 4);
@@ -349,24 +510,20 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
                    "r"(w[2]), "r"(w[3])
                    : "memory");
     }
-    {
-      const uint64_t sl = ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
-      const uint64_t sp = ptx::fadd2(ptx::fadd2(acc_lp[0], acc_lp[1]),
-                                     ptx::fadd2(acc_lp[2], acc_lp[3]));
-      float a0, a1, b0, b1;
-      ptx::f2unpack(sl, a0, a1);
-      ptx::f2unpack(sp, b0, b1);
-      l += a0 + a1;
-      lp += b0 + b1;
-    }
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     ptx::mbar_arrive(bar(L::bPFull + t));
+    if (r == 0) DIT_TRACE(kTrSmArrive0 + 5 * t, j);
+    {
+      const uint64_t sl = ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
+      float a0, a1;
+      ptx::f2unpack(sl, a0, a1);
+      l += a0 + a1;
+      lp += ((acc_lp[0] + acc_lp[1]) + (acc_lp[2] + acc_lp[3])) +
+            ((acc_lp[4] + acc_lp[5]) + (acc_lp[6] + acc_lp[7]));
+    }
   }
-  if (ok) {
-    ok = wait_or_abort(bar(L::bODone), 0, abort_flag, p.wait_limit);
-    ok = __all_sync(0xffffffffu, ok);
-  }
+  if (ok) ok = wait(L::bPVDone + t, (n_tiles - 1) & 1);
   if (!ok) {
     raise_abort(p, abort_flag);
     return;
@@ -429,15 +586,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
     ptx::mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(bar(L::bKVFull + s), 1);
+      ptx::mbar_init(bar(L::bKFull + s), 1);
+      ptx::mbar_init(bar(L::bVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(L::bSFull + t), 1);
+      ptx::mbar_init(bar(L::bSEmpty + t), kBlockM);
       ptx::mbar_init(bar(L::bPFull + t), kBlockM);
+      ptx::mbar_init(bar(L::bPVDone + t), 1);
     }
-    ptx::mbar_init(bar(L::bODone), 1);
-    ptx::mbar_init(bar(L::bDrain), 1);
+    ptx::mbar_init(bar(L::bDrainS), 1);
+    ptx::mbar_init(bar(L::bDrainPV), 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -458,7 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == kLoadWarp) {
     if (lane == 0) detail::producer<D>(p, sbase, bh, q_row0, n_tiles, abort_flag);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) detail::mma_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+    if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
     __syncwarp();
   } else {
     detail::softmax_epilogue<D, kOutF32>(p, sbase, tmem, warp >> 2, warp, lane, bh, q_row0,
