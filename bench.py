@@ -409,7 +409,7 @@ def run_gpu(args):
                          "peak_kind": f"{peak_src} bf16 sustained",
                          "frac_of_burst_peak": fused_tflops / peak_burst,
                          "traffic": traffic,
-                         "algorithmic_bytes": 4 * B * H * N * D * 2 + B * H * N * (D * 4 + 4)},
+                         "algorithmic_bytes": 3 * B * H * N * D * 2 + B * H * N * (D * 4 + 4)},
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
