@@ -68,8 +68,10 @@ namespace ditattn {
 enum TraceEvent {
   kTrProdEmpty = 0, kTrProdIssue, kTrMmaK, kTrMmaS0, kTrMmaS1, kTrMmaV, kTrMmaP0, kTrMmaPv0,
   kTrMmaP1, kTrMmaPv1, kTrSmFull0, kTrSmLd0, kTrSmMax0, kTrSmExp0, kTrSmArrive0,
-  kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1
+  kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1, kTrCta
 };
+// kTrCta slots (tile index): 0 start, 1 first S ready (tile 0), 2 epilogue start,
+// 3 epilogue end (tile 0 warpgroup), 4 CTA exit.
 
 constexpr int kBlockM = 128;              // query rows per Q tile (two per CTA)
 constexpr int kBlockN = 128;              // keys per KV tile
@@ -86,6 +88,7 @@ struct AttnParams {
   CUtensorMap tm_q;   // (D, n_q, bh) bf16, box (64, 128, 1), 128B swizzle
   CUtensorMap tm_k;   // (D, n_kv, bh), head stride = kv_head_stride
   CUtensorMap tm_v;
+  CUtensorMap tm_o;   // (D, n_q, bh) fp32 or bf16, box (128 bytes, 128, 1), 128B swizzle (stores)
   void* out;          // [bh, n_q, D] fp32 or bf16
   float* lse;         // [bh, n_q]
   int* status;        // device status word (timeouts)
@@ -408,6 +411,7 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
   for (int j = 0; j < n_tiles; ++j) {
     if (!(ok = wait(L::bSFull + t, j & 1))) break;
     if (r == 0) DIT_TRACE(kTrSmFull0 + 5 * t, j);
+    if (r == 0 && t == 0 && j == 0) DIT_TRACE(kTrCta, 1);
     ptx::tc_fence_after();
 
     float s[kBlockN];
@@ -529,42 +533,69 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
     return;
   }
   ptx::tc_fence_after();
+  if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2);
 
   const int row = q_row0 + t * kBlockM + r;
   const bool store = row < p.n_q;
   // O is normalised by the sum of the rounded weights it was built from, so the weights
   // sum to one; the LSE uses the unrounded sum.
   const float inv_l = 1.f / lp;
-  const size_t out_row = (static_cast<size_t>(bh) * p.n_q + row) * D;
+  // Stage the normalised O tile in shared memory as 128-byte-wide swizzled boxes (the
+  // P_t buffer, then Q_t: both are free once the tile's last MMAs have completed) and
+  // write it with TMA stores; rows past n_q are clipped by the tensor map.
+  constexpr int kEs = kOutF32 ? 4 : 2;
+  constexpr int kBoxCols = 128 / kEs;  // elements per 128-byte box row
+  constexpr int kBoxes = D / kBoxCols;
+  const uint32_t sQt = sbase + (t ? L::kQ1 : L::kQ0);
+  auto box_base = [&](int b) { return (b < 2 ? sP : sQt) + (b & 1) * L::kRegion; };
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t u[32];
     ptx::tmem_ld32(tO + cc * 32, u);
     ptx::tmem_wait_ld();
-    if (store) {
-      if constexpr (kOutF32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + out_row + cc * 32);
+    if constexpr (kOutF32) {
+      const uint32_t rowp = box_base(cc) + r * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          dst[i] = make_float4(__uint_as_float(u[4 * i + 0]) * inv_l,
-                               __uint_as_float(u[4 * i + 1]) * inv_l,
-                               __uint_as_float(u[4 * i + 2]) * inv_l,
-                               __uint_as_float(u[4 * i + 3]) * inv_l);
-      } else {
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + out_row + cc * 32);
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = rowp + ((static_cast<uint32_t>(c) ^ sw) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "f"(__uint_as_float(u[4 * c + 0]) * inv_l),
+                     "f"(__uint_as_float(u[4 * c + 1]) * inv_l),
+                     "f"(__uint_as_float(u[4 * c + 2]) * inv_l),
+                     "f"(__uint_as_float(u[4 * c + 3]) * inv_l)
+                     : "memory");
+      }
+    } else {
+      const uint32_t rowp = box_base(cc / 2) + r * 128;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          uint4 w;
-          w.x = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv_l, __uint_as_float(u[8 * i + 1]) * inv_l);
-          w.y = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l, __uint_as_float(u[8 * i + 3]) * inv_l);
-          w.z = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l, __uint_as_float(u[8 * i + 5]) * inv_l);
-          w.w = ptx::pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l, __uint_as_float(u[8 * i + 7]) * inv_l);
-          dst[i] = w;
-        }
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = static_cast<uint32_t>((cc % 2) * 4 + i);
+        const uint32_t addr = rowp + ((c ^ sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv_l,
+                                          __uint_as_float(u[8 * i + 1]) * inv_l)),
+                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l,
+                                          __uint_as_float(u[8 * i + 3]) * inv_l)),
+                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l,
+                                          __uint_as_float(u[8 * i + 5]) * inv_l)),
+                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l,
+                                          __uint_as_float(u[8 * i + 7]) * inv_l))
+                     : "memory");
       }
     }
   }
+  ptx::fence_proxy_async_smem();
+  ptx::named_barrier(1 + t, kBlockM);
+  if (r == 0 && q_row0 + t * kBlockM < p.n_q) {  // a tile wholly past n_q stores nothing
+#pragma unroll
+    for (int b = 0; b < kBoxes; ++b)
+      ptx::tma_store_3d(&p.tm_o, box_base(b), b * kBoxCols, q_row0 + t * kBlockM, bh);
+    ptx::bulk_commit_group();
+    ptx::bulk_wait_reads();  // the staging buffers may be released
+  }
   if (store) p.lse[static_cast<size_t>(bh) * p.n_q + row] = (m + log2f(l)) * 0.69314718055994530942f;
+  if (r == 0 && t == 0) DIT_TRACE(kTrCta, 3);
 }
 
 }  // namespace detail
@@ -605,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::tma_prefetch_desc(&p.tm_q);
     ptx::tma_prefetch_desc(&p.tm_k);
     ptx::tma_prefetch_desc(&p.tm_v);
+    ptx::tma_prefetch_desc(&p.tm_o);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(sbase + L::kTmemSlot, 512);
@@ -614,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
+  if (threadIdx.x == 0) DIT_TRACE(kTrCta, 0);
 
   if (warp == kLoadWarp) {
     if (lane == 0) detail::producer<D>(p, sbase, bh, q_row0, n_tiles, abort_flag);
@@ -634,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
+  if (threadIdx.x == 0) DIT_TRACE(kTrCta, 4);
 }
 
 }  // namespace ditattn

@@ -8,8 +8,10 @@
 // D*sizeof(out) + 4 bytes per query row.  Each thread owns one 16-byte vector
 // of one row (4 fp32 or 8 bf16 partial elements); the threads of a row are
 // consecutive, so every partial row is read by fully coalesced 16-byte
-// streaming loads, and a batch of up to 8 chunks' loads is issued before any
-// of them is used.
+// streaming loads.  Chunks are taken in batches of up to 8: all loads of a
+// batch (LSEs and partial vectors) are issued before any arithmetic, and the
+// batches are combined online (running max M, running sum S of exp(lse_c - M),
+// running weighted sum A), then O = A / S and lse = M + ln S.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -29,20 +31,24 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <typename T> struct Vec;
 template <> struct Vec<float> {
   static constexpr int kN = 4;
-  __device__ static void load(const float* p, float (&x)[4]) {
-    const float4 v = __ldcs(reinterpret_cast<const float4*>(p));
+  using Raw = float4;
+  __device__ static Raw load(const float* p) { return __ldcs(reinterpret_cast<const float4*>(p)); }
+  __device__ static void widen(const Raw& v, float (&x)[4]) {
     x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
   }
 };
 template <> struct Vec<__nv_bfloat16> {
   static constexpr int kN = 8;
-  __device__ static void load(const __nv_bfloat16* p, float (&x)[8]) {
-    const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p));
+  using Raw = uint4;
+  __device__ static Raw load(const __nv_bfloat16* p) {
+    return __ldcs(reinterpret_cast<const uint4*>(p));
+  }
+  __device__ static void widen(const Raw& v, float (&x)[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      x[2 * i] = ptx::bf16lo(w[i]);
+      x[2 * i + 1] = ptx::bf16hi(w[i]);
     }
   }
 };
@@ -75,7 +81,7 @@ __device__ __forceinline__ void store_out(__nv_bfloat16* dst, const float (&a)[N
 }
 
 template <typename PT, typename OT, int D>
-__global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(
+__global__ void __launch_bounds__(kMergeThreads, 4) lse_merge_kernel(
     const PT* __restrict__ partials, const float* __restrict__ lses, int p, long long rows,
     OT* __restrict__ out, float* __restrict__ lse_out) {
   constexpr int kV = Vec<PT>::kN;
@@ -84,38 +90,57 @@ __global__ void __launch_bounds__(kMergeThreads) lse_merge_kernel(
   const long long row = gt / kTpr;
   if (row >= rows) return;
   const int col = static_cast<int>(gt % kTpr) * kV;
+  const PT* base = partials + row * D + col;
+  const long long cstride = rows * D;
 
-  float M = -INFINITY;
-  for (int c = 0; c < p; ++c) M = fmaxf(M, __ldg(lses + c * rows + row));
-  float acc[kV];
+  float M = -INFINITY;  // running max of the LSEs seen so far
+  float S = 0.f;        // running sum of exp(lse_c - M)
+  float acc[kV];        // running sum of exp(lse_c - M) * O_c
 #pragma unroll
   for (int i = 0; i < kV; ++i) acc[i] = 0.f;
+
+  for (int c0 = 0; c0 < p; c0 += kBatch) {
+    typename Vec<PT>::Raw raw[kBatch];
+    float lv[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (c0 + b < p) {
+        lv[b] = __ldg(lses + (c0 + b) * rows + row);
+        raw[b] = Vec<PT>::load(base + (c0 + b) * cstride);
+      } else {
+        lv[b] = -INFINITY;
+      }
+    }
+    float mb = lv[0];
+#pragma unroll
+    for (int b = 1; b < kBatch; ++b) mb = fmaxf(mb, lv[b]);
+    const float Mn = fmaxf(M, mb);
+    if (Mn == -INFINITY) continue;  // nothing but empty chunks so far
+    const float r = ptx::ex2_approx((M - Mn) * kLog2e);  // 0 while M = -inf
+    S *= r;
+#pragma unroll
+    for (int i = 0; i < kV; ++i) acc[i] *= r;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (c0 + b < p) {
+        const float w = ptx::ex2_approx((lv[b] - Mn) * kLog2e);  // 0 for an empty chunk
+        float x[kV];
+        Vec<PT>::widen(raw[b], x);
+        S += w;
+#pragma unroll
+        for (int i = 0; i < kV; ++i) acc[i] = fmaf(w, x[i], acc[i]);
+      }
+    }
+    M = Mn;
+  }
   float L = -INFINITY;
   if (M != -INFINITY) {
-    float sum = 0.f;
-    for (int c = 0; c < p; ++c) sum += ptx::ex2_approx((__ldg(lses + c * rows + row) - M) * kLog2e);
+    const float inv = 1.f / S;
+#pragma unroll
+    for (int i = 0; i < kV; ++i) acc[i] *= inv;
     float lg;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(sum));
+    asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(S));
     L = M + lg * kLn2;
-    const PT* base = partials + row * D + col;
-    const long long cstride = rows * D;
-    for (int c0 = 0; c0 < p; c0 += kBatch) {
-      float x[kBatch][kV];
-      float w[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        if (c0 + b < p) {
-          Vec<PT>::load(base + (c0 + b) * cstride, x[b]);
-          w[b] = ptx::ex2_approx((__ldg(lses + (c0 + b) * rows + row) - L) * kLog2e);
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b)
-        if (c0 + b < p) {
-#pragma unroll
-          for (int i = 0; i < kV; ++i) acc[i] = fmaf(w[b], x[b][i], acc[i]);
-        }
-    }
   }
   store_out(out + row * D + col, acc);
   if (col == 0) lse_out[row] = L;
