@@ -14,6 +14,22 @@ namespace {
 // Test-only failure injection (dit_test_inject_stall).
 int g_stall_kv = 0;
 long long g_wait_limit = kDefaultWaitLimit;
+// Test-only cap on the persistent grid (0: one CTA per SM).
+int g_grid_limit = 0;
+
+// Streaming multiprocessors of the current device, cached per device.
+int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -76,7 +92,12 @@ cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
   auto kern = attn_fwd_kernel<D, kF32>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(prm.q_pairs) * static_cast<unsigned>(prm.bh_count));
+  // Persistent grid: one CTA per SM (shared memory and TMEM allow no more), each
+  // walking work items blockIdx.x, blockIdx.x + gridDim.x, ...
+  int ctas = sm_count();
+  if (g_grid_limit > 0 && g_grid_limit < ctas) ctas = g_grid_limit;
+  if (prm.num_items < ctas) ctas = prm.num_items;
+  const dim3 grid(static_cast<unsigned>(ctas));
   kern<<<grid, kThreads, kSmem, st>>>(prm);
   return cudaGetLastError();
 }
@@ -90,19 +111,21 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
       !encode_bhnd(&prm.tm_v, a.v, a.d, a.n_kv, a.bh, a.kv_head_stride) ||
       !encode_out(&prm.tm_o, a.out, a.d, a.n_q, a.bh, a.out_f32))
     return cudaErrorInvalidValue;
-  prm.out = a.out;
   prm.lse = a.lse;
   prm.status = a.status;
   prm.n_q = a.n_q;
   prm.n_kv = a.n_kv;
   prm.bh_count = a.bh;
   prm.q_pairs = (a.n_q + 2 * kBlockM - 1) / (2 * kBlockM);
+  prm.num_items = prm.q_pairs * a.bh;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;
   prm.stall_kv = g_stall_kv;
   if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
   return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);
 }
+
+void set_grid_limit(int max_ctas) { g_grid_limit = max_ctas > 0 ? max_ctas : 0; }
 
 void set_stall_injection(int enable, long long wait_limit_cycles) {
   g_stall_kv = enable ? 1 : 0;

@@ -1,7 +1,7 @@
 // Fused non-causal attention forward for sm_103a: tcgen05 MMA with TMEM
 // accumulators, TMA-staged bf16 tiles, fp32 online softmax.
 //
-// Computes, per head bh and query row i of the CTA's two 128-row Q tiles,
+// Computes, per head bh and query row i,
 //   o_i = sum_j softmax_j(scale * q_i . k_j) v_j   over key rows j in [0, n_kv)
 //   lse_i = ln sum_j exp(scale * q_i . k_j)
 // (MindIE-SD parallelism docs, "Ring Sequence Parallel" usage example: local
@@ -10,10 +10,15 @@
 // the fused pass (n_kv = N) and one KV chunk of the ring decomposition (K/V
 // pointers offset to the chunk, n_kv = chunk length, explicit head stride).
 //
-// CTA organisation (352 threads, one CTA per SM):
-//   warps 0-3  softmax for Q tile 0   (thread = query row = TMEM lane)
-//   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer (Q once, then K/V tiles through a 3-slot ring)
+// Persistent: one CTA per SM walks work items (head bh, pair of 128-row Q tiles)
+// w = blockIdx.x, blockIdx.x + gridDim.x, ...  (head-major, so the CTAs resident at
+// any moment share a head's K/V in L2).  Every barrier's phase count runs on across
+// items, so the next item's Q load and first S MMAs overlap this item's epilogue.
+//
+// CTA organisation (352 threads):
+//   warps 0-3  softmax + epilogue for Q tile 0   (thread = query row = TMEM lane)
+//   warps 4-7  softmax + epilogue for Q tile 1
+//   warp  8    TMA producer (Q per item, then K/V tiles through a 3-slot ring)
 //   warp  9    TMEM allocator + single-thread issuer of S = Q K^T
 //   warp 10    single-thread issuer of O += P V
 // Two issuers keep the tensor pipe fed: its queue is about one instruction deep,
@@ -21,16 +26,18 @@
 // one issuer waits the other issues.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, fp32, lane = query row.
 // Shared memory: Q0, Q1, P0, P1 (bf16 probabilities, written by the softmax
-// warps in the 128-byte-swizzled K-major layout the MMA reads) and the K/V ring.
+// warps in the 128-byte-swizzled K-major layout the MMA reads; P_t also stages
+// the O tile for its TMA store) and the K/V ring.
 //
 // Pipeline.  A softmax warpgroup releases its S buffer (S_EMPTY) as soon as
-// the scores are in registers, so the MMA warp computes S_t(j+1) = Q_t K_{j+1}^T
-// while softmax t is still turning S_t(j) into probabilities; softmax t can
-// start tile j+1 the moment it has published P_t(j) (P_FULL).  O_t += P_t(j) V_j
-// is committed to its own barrier (PV_DONE), which softmax t waits on only
-// before it rescales O_t or overwrites the P_t buffer.  Per KV tile the S issuer
-// issues S0(j+1), S1(j+1) and the PV issuer PV0(j), PV1(j); the K/V ring is filled
-// in consumption order: K0, K1, V0, K2, V1, ...
+// the scores are in registers, so the S issuer computes S_t(g+1) = Q_t K^T while
+// softmax t is still turning S_t(g) into probabilities; softmax t starts the next
+// tile the moment it has published P_t(g) (P_FULL).  O_t += P_t V is committed to
+// its own barrier (PV_DONE), which softmax t waits on only before it rescales O_t
+// or overwrites the P_t buffer.  Q_EMPTY (last S MMA of an item done) lets the
+// producer refill Q; O_EMPTY (epilogue has read O_t) lets the PV issuer start the
+// next item's O_t.  The K/V ring is filled in consumption order: K0, K1, V0, K2,
+// V1, ... per item.
 //
 // Online softmax (base 2, scale folded into log2e): the running max m is only
 // raised when a tile's max exceeds it by more than kRescaleLog2 (then O and the
@@ -70,10 +77,11 @@ enum TraceEvent {
   kTrMmaP1, kTrMmaPv1, kTrSmFull0, kTrSmLd0, kTrSmMax0, kTrSmExp0, kTrSmArrive0,
   kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1, kTrCta
 };
-// kTrCta slots (tile index): 0 start, 1 first S ready (tile 0), 2 epilogue start,
-// 3 epilogue end (tile 0 warpgroup), 4 CTA exit.
+// Per-tile events are indexed by the CTA-global tile count; kTrCta slots: 0 start,
+// 1 first S seen, then per item i: 2 + 2i epilogue start, 3 + 2i epilogue end
+// (tile-0 warpgroup); 63 CTA exit.
 
-constexpr int kBlockM = 128;              // query rows per Q tile (two per CTA)
+constexpr int kBlockM = 128;              // query rows per Q tile (two per work item)
 constexpr int kBlockN = 128;              // keys per KV tile
 constexpr int kStages = 3;                // K/V ring slots
 constexpr int kThreads = 352;
@@ -89,13 +97,13 @@ struct AttnParams {
   CUtensorMap tm_k;   // (D, n_kv, bh), head stride = kv_head_stride
   CUtensorMap tm_v;
   CUtensorMap tm_o;   // (D, n_q, bh) fp32 or bf16, box (128 bytes, 128, 1), 128B swizzle (stores)
-  void* out;          // [bh, n_q, D] fp32 or bf16
   float* lse;         // [bh, n_q]
   int* status;        // device status word (timeouts)
   int n_q;
   int n_kv;
   int bh_count;
   int q_pairs;        // ceil(n_q / 256)
+  int num_items;      // bh_count * q_pairs
   float scale_log2;   // scale * log2(e)
   long long wait_limit;  // SM clocks a bounded wait may spin before giving up
   int stall_kv;          // test-only failure injection: never issue K/V copies
@@ -114,15 +122,17 @@ struct AttnSmem {
   static constexpr uint32_t kKV = kP1 + kPTile;
   static constexpr uint32_t kBars = kKV + kStages * kTile;
   // barrier indices
-  static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;                   // + slot: a K tile landed in the slot
+  static constexpr int bQFull = 0;                   // Q tiles of an item landed
+  static constexpr int bQEmpty = 1;                  // last S MMA of an item done (MMA commit)
+  static constexpr int bKFull = 2;                   // + slot: a K tile landed in the slot
   static constexpr int bVFull = bKFull + kStages;    // + slot: a V tile landed in the slot
   static constexpr int bKVEmpty = bVFull + kStages;  // + slot: the slot's tile was consumed
   static constexpr int bSFull = bKVEmpty + kStages;  // + tile: S_t computed (MMA commit)
   static constexpr int bSEmpty = bSFull + 2;         // + tile: S_t read into registers (128 arrivals)
   static constexpr int bPFull = bSEmpty + 2;         // + tile: P_t written (128 arrivals)
   static constexpr int bPVDone = bPFull + 2;         // + tile: O_t += P_t V done (MMA commit)
-  static constexpr int bDrainS = bPVDone + 2;        // abort drain, S issuer
+  static constexpr int bOEmpty = bPVDone + 2;        // + tile: O_t read by the epilogue (128 arrivals)
+  static constexpr int bDrainS = bOEmpty + 2;        // abort drain, S issuer
   static constexpr int bDrainPV = bDrainS + 1;       // abort drain, PV issuer
   static constexpr int kNumBars = bDrainPV + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
@@ -151,30 +161,33 @@ __device__ __forceinline__ void raise_abort(const AttnParams& p, volatile int* a
   atomicOr(p.status, kStatusTimeout);
 }
 
-// K/V ring items in consumption order: K_0, then per KV tile j: K_{j+1} (if any), V_j.
-// Item i goes to slot i % kStages.  K and V tiles landing in a slot complete different
-// barriers (K_FULL / V_FULL), so each MMA issuer observes the phases of only the
-// barriers it consumes, in order, and can never mistake an older fill for a newer one.
+struct Item {
+  int bh;
+  int q_row0;
+};
+__device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
+  return {w / p.q_pairs, (w % p.q_pairs) * 2 * kBlockM};
+}
+
+// K/V ring items of one work item, in consumption order: K_0, then per KV tile j:
+// K_{j+1} (if any), V_j.  Ring index i goes to slot i % kStages; the ring index runs on
+// across work items (2 * n_tiles per item).  K and V tiles landing in a slot complete
+// different barriers (K_FULL / V_FULL), so each MMA issuer observes the phases of only
+// the barriers it consumes, in order, and can never mistake an older fill for a newer one.
+__device__ __forceinline__ int k_item(int j) { return j == 0 ? 0 : 2 * j - 1; }
 __device__ __forceinline__ int v_item(int j, int n_tiles) {
   return (j + 1 < n_tiles) ? 2 * j + 2 : 2 * j + 1;
 }
 
 template <int D>
-__device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, int bh, int q_row0,
-                                         int n_tiles, volatile int* abort_flag) {
+__device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, int n_tiles,
+                                         volatile int* abort_flag) {
   using L = AttnSmem<D>;
   constexpr int kRegions = D / 64;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-
-  ptx::mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
-#pragma unroll
-  for (int t = 0; t < 2; ++t)
-#pragma unroll
-    for (int r = 0; r < kRegions; ++r)
-      ptx::tma_load_3d(sbase + (t ? L::kQ1 : L::kQ0) + r * L::kRegion, &p.tm_q, bar(L::bQFull),
-                       r * 64, q_row0 + t * kBlockM, bh);
-
-  if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
+  auto wait = [&](int b, uint32_t parity) {
+    return wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
+  };
 
   uint32_t kpar = 0, vpar = 0;  // bit s: parity of the next K_FULL[s] / V_FULL[s] phase
   int last_bar[kStages];        // barrier and parity of the newest copy into each slot
@@ -184,11 +197,13 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     last_bar[s] = -1;
     last_par[s] = 0;
   }
-  int it = 0;
-  auto load = [&](bool is_v, int tile) {
+  int q_loads = 0;  // Q loads issued (QFULL phases armed)
+  int it = 0;       // ring index
+  bool ok = true;
+  auto load = [&](bool is_v, int tile, int bh) {
     const int s = it % kStages;
     const uint32_t ph = (it / kStages) & 1;
-    if (!wait_or_abort(bar(L::bKVEmpty + s), ph ^ 1, abort_flag, p.wait_limit)) return false;
+    if (!wait(L::bKVEmpty + s, ph ^ 1)) return false;
     DIT_TRACE(kTrProdEmpty, it);
     const int fb = (is_v ? L::bVFull : L::bKFull) + s;
     const uint32_t par = ((is_v ? vpar : kpar) >> s) & 1;
@@ -209,15 +224,31 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     ++it;
     return true;
   };
-  bool ok = load(false, 0);
-  for (int j = 0; ok && j < n_tiles; ++j) {
-    if (j + 1 < n_tiles && !(ok = load(false, j + 1))) break;
-    ok = load(true, j);
+
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x) {
+    const Item item = item_of(p, w);
+    // Q_t is free once the previous item's last S MMAs have completed.
+    if (!(ok = wait(L::bQEmpty, (q_loads & 1) ^ 1))) break;
+    ptx::mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int r = 0; r < kRegions; ++r)
+        ptx::tma_load_3d(sbase + (t ? L::kQ1 : L::kQ0) + r * L::kRegion, &p.tm_q,
+                         bar(L::bQFull), r * 64, item.q_row0 + t * kBlockM, item.bh);
+    ++q_loads;
+    if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
+
+    if (!(ok = load(false, 0, item.bh))) break;
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      if (j + 1 < n_tiles && !(ok = load(false, j + 1, item.bh))) break;
+      ok = load(true, j, item.bh);
+    }
   }
   if (!ok) {
     raise_abort(p, abort_flag);
     // Let every copy this thread started land before the CTA can exit.
-    ptx::mbar_wait(bar(L::bQFull), 0, p.wait_limit);
+    if (q_loads > 0) ptx::mbar_wait(bar(L::bQFull), (q_loads - 1) & 1, p.wait_limit);
 #pragma unroll
     for (int s = 0; s < kStages; ++s)
       if (last_bar[s] >= 0) ptx::mbar_wait(bar(last_bar[s]), last_par[s], p.wait_limit);
@@ -259,7 +290,7 @@ struct Descs {
   }
 };
 
-// S_t = Q_t K^T for every KV tile (warp kMmaWarp, one thread).
+// S_t = Q_t K^T for every KV tile of every work item (warp kMmaWarp, one thread).
 template <int D>
 __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                          int n_tiles, volatile int* abort_flag) {
@@ -282,37 +313,34 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
   auto wait = [&](int b, uint32_t parity) {
     return wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
   };
-  uint32_t kpar = 0;  // bit s: parity of the next K_FULL[s] phase
-  auto wait_k = [&](int s) {
-    const bool r = wait(L::bKFull + s, (kpar >> s) & 1);
-    kpar ^= 1u << s;
-    return r;
-  };
 
-  bool ok = wait(L::bQFull, 0) && wait_k(0);
-  if (ok) {
-    ptx::tc_fence_after();
-    issue(0, 0);
-    ptx::mma_commit(bar(L::bSFull + 0));
-    issue(1, 0);
-    ptx::mma_commit(bar(L::bSFull + 1));
-    ptx::mma_commit(bar(L::bKVEmpty + 0));
-  }
-  for (int j = 0; ok && j + 1 < n_tiles; ++j) {
-    const int sK = (2 * j + 1) % kStages;  // ring item of K_{j+1}
-    if (!(ok = wait_k(sK))) break;
-    DIT_TRACE(kTrMmaK, j);
-    if (!(ok = wait(L::bSEmpty + 0, j & 1))) break;
-    ptx::tc_fence_after();
-    issue(0, sK);
-    ptx::mma_commit(bar(L::bSFull + 0));
-    DIT_TRACE(kTrMmaS0, j);
-    if (!(ok = wait(L::bSEmpty + 1, j & 1))) break;
-    ptx::tc_fence_after();
-    issue(1, sK);
-    ptx::mma_commit(bar(L::bSFull + 1));
-    ptx::mma_commit(bar(L::bKVEmpty + sK));
-    DIT_TRACE(kTrMmaS1, j);
+  uint32_t kpar = 0;  // bit s: parity of the next K_FULL[s] phase
+  int g = 0;          // S tiles issued per Q tile (CTA-global)
+  int li = 0;         // work items started
+  int ring0 = 0;      // ring index of this item's first K/V tile
+  bool ok = true;
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li, ring0 += 2 * n_tiles) {
+    if (!(ok = wait(L::bQFull, li & 1))) break;
+    for (int j = 0; j < n_tiles; ++j, ++g) {
+      const int sK = (ring0 + k_item(j)) % kStages;
+      ok = wait(L::bKFull + sK, (kpar >> sK) & 1);
+      kpar ^= 1u << sK;
+      if (!ok) break;
+      DIT_TRACE(kTrMmaK, g);
+      // S_t(g) overwrites S_t: softmax t must have loaded S_t(g-1).
+      if (g > 0 && !(ok = wait(L::bSEmpty + 0, (g - 1) & 1))) break;
+      ptx::tc_fence_after();
+      issue(0, sK);
+      ptx::mma_commit(bar(L::bSFull + 0));
+      DIT_TRACE(kTrMmaS0, g);
+      if (g > 0 && !(ok = wait(L::bSEmpty + 1, (g - 1) & 1))) break;
+      ptx::tc_fence_after();
+      issue(1, sK);
+      ptx::mma_commit(bar(L::bSFull + 1));
+      ptx::mma_commit(bar(L::bKVEmpty + sK));
+      DIT_TRACE(kTrMmaS1, g);
+    }
+    if (ok) ptx::mma_commit(bar(L::bQEmpty));  // Q_0/Q_1 free once these MMAs are done
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -322,7 +350,7 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
   }
 }
 
-// O_t += P_t V_j for every KV tile (warp kPvWarp, one thread).
+// O_t += P_t V_j for every KV tile of every work item (warp kPvWarp, one thread).
 template <int D>
 __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                           int n_tiles, volatile int* abort_flag) {
@@ -344,28 +372,36 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
   auto wait = [&](int b, uint32_t parity) {
     return wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
   };
-  uint32_t vpar = 0;  // bit s: parity of the next V_FULL[s] phase
 
+  uint32_t vpar = 0;  // bit s: parity of the next V_FULL[s] phase
+  int g = 0;          // PV tiles issued per Q tile (CTA-global)
+  int li = 0;
+  int ring0 = 0;
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    const int sV = v_item(j, n_tiles) % kStages;
-    if (!(ok = wait(L::bPFull + 0, j & 1))) break;
-    DIT_TRACE(kTrMmaP0, j);
-    ok = wait(L::bVFull + sV, (vpar >> sV) & 1);
-    vpar ^= 1u << sV;
-    if (!ok) break;
-    DIT_TRACE(kTrMmaV, j);
-    ptx::tc_fence_after();
-    issue(0, sV, j > 0);
-    ptx::mma_commit(bar(L::bPVDone + 0));
-    DIT_TRACE(kTrMmaPv0, j);
-    if (!(ok = wait(L::bPFull + 1, j & 1))) break;
-    DIT_TRACE(kTrMmaP1, j);
-    ptx::tc_fence_after();
-    issue(1, sV, j > 0);
-    ptx::mma_commit(bar(L::bPVDone + 1));
-    ptx::mma_commit(bar(L::bKVEmpty + sV));
-    DIT_TRACE(kTrMmaPv1, j);
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li, ring0 += 2 * n_tiles) {
+    for (int j = 0; j < n_tiles; ++j, ++g) {
+      const int sV = (ring0 + v_item(j, n_tiles)) % kStages;
+      if (!(ok = wait(L::bPFull + 0, g & 1))) break;
+      DIT_TRACE(kTrMmaP0, g);
+      ok = wait(L::bVFull + sV, (vpar >> sV) & 1);
+      vpar ^= 1u << sV;
+      if (!ok) break;
+      DIT_TRACE(kTrMmaV, g);
+      // The first PV of an item overwrites O_t: the previous item's epilogue must have read it.
+      if (j == 0 && li > 0 && !(ok = wait(L::bOEmpty + 0, (li - 1) & 1))) break;
+      ptx::tc_fence_after();
+      issue(0, sV, j > 0);
+      ptx::mma_commit(bar(L::bPVDone + 0));
+      DIT_TRACE(kTrMmaPv0, g);
+      if (!(ok = wait(L::bPFull + 1, g & 1))) break;
+      DIT_TRACE(kTrMmaP1, g);
+      if (j == 0 && li > 0 && !(ok = wait(L::bOEmpty + 1, (li - 1) & 1))) break;
+      ptx::tc_fence_after();
+      issue(1, sV, j > 0);
+      ptx::mma_commit(bar(L::bPVDone + 1));
+      ptx::mma_commit(bar(L::bKVEmpty + sV));
+      DIT_TRACE(kTrMmaPv1, g);
+    }
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -386,9 +422,8 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
 
 template <int D, bool kOutF32>
 __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t sbase,
-                                                 uint32_t tmem, int t, int warp, int lane, int bh,
-                                                 int q_row0, int n_tiles,
-                                                 volatile int* abort_flag) {
+                                                 uint32_t tmem, int t, int warp, int lane,
+                                                 int n_tiles, volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int quarter = warp & 3;
@@ -397,6 +432,7 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
   const uint32_t tS = tmem + t * kBlockN + lane_off;
   const uint32_t tO = tmem + 2 * kBlockN + t * D + lane_off;
   const uint32_t sP = sbase + (t ? L::kP1 : L::kP0);
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
   const float c = p.scale_log2;
   // Warp-uniform bounded wait.
   auto wait = [&](int b, uint32_t parity) {
@@ -404,198 +440,222 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
     return __all_sync(0xffffffffu, ok);
   };
 
-  float m = -INFINITY;  // running max of scale*log2e*s (possibly stale by < 2^8)
-  float l = 0.f;        // running sum of 2^(c*s - m), for the LSE
-  float lp = 0.f;       // running sum of the bf16-rounded P the PV GEMM sees, for O
+  int g = 0;   // tiles processed by this warpgroup (CTA-global)
+  int li = 0;  // work items processed
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    if (!(ok = wait(L::bSFull + t, j & 1))) break;
-    if (r == 0) DIT_TRACE(kTrSmFull0 + 5 * t, j);
-    if (r == 0 && t == 0 && j == 0) DIT_TRACE(kTrCta, 1);
-    ptx::tc_fence_after();
-
-    float s[kBlockN];
-#pragma unroll
-    for (int cc = 0; cc < kBlockN / 32; ++cc) {
-      uint32_t u[32];
-      ptx::tmem_ld32(tS + cc * 32, u);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
-    }
-    ptx::tmem_wait_ld();
-    // S_t is in registers: the MMA warp may overwrite it with S_t(j+1).
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(L::bSEmpty + t));
-    if (r == 0) DIT_TRACE(kTrSmLd0 + 5 * t, j);
-
-    const int valid = p.n_kv - j * kBlockN;
-    if (valid < kBlockN) {
-#pragma unroll
-      for (int i = 0; i < kBlockN; ++i)
-        if (i >= valid) s[i] = -INFINITY;
-    }
-    // Tile row max: 8 independent 3-input max chains, then a short tree.
-    float mx;
-    {
-      float a[8];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        a[g] = ptx::fmax3(s[16 * g], s[16 * g + 1], s[16 * g + 2]);
-#pragma unroll
-        for (int i = 3; i < 15; i += 2) a[g] = ptx::fmax3(a[g], s[16 * g + i], s[16 * g + i + 1]);
-        a[g] = fmaxf(a[g], s[16 * g + 15]);
-      }
-      mx = ptx::fmax3(ptx::fmax3(a[0], a[1], a[2]), ptx::fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
-    }
-    if (r == 0) DIT_TRACE(kTrSmMax0 + 5 * t, j);
-    const float m_tile = mx * c;
-    const bool raise = m_tile > m + kRescaleLog2;  // always true on the first tile
-    float alpha = 1.f;
-    if (raise) {
-      alpha = ptx::ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
-      m = m_tile;
-    }
-    l *= alpha;
-    lp *= alpha;
-    bool pv_prev_done = (j == 0);
-    if (j > 0 && __any_sync(0xffffffffu, raise)) {
-      // O_t may only be touched once PV_t(j-1) has landed.
-      if (!(ok = wait(L::bPVDone + t, (j - 1) & 1))) break;
-      pv_prev_done = true;
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
+    const Item item = item_of(p, w);
+    float m = -INFINITY;  // running max of scale*log2e*s (possibly stale by < 2^8)
+    float l = 0.f;        // running sum of 2^(c*s - m), for the LSE
+    float lp = 0.f;       // running sum of the bf16-rounded P the PV GEMM sees, for O
+    for (int j = 0; j < n_tiles; ++j, ++g) {
+      if (!(ok = wait(L::bSFull + t, g & 1))) break;
+      if (r == 0) DIT_TRACE(kTrSmFull0 + 5 * t, g);
+      if (r == 0 && t == 0 && g == 0) DIT_TRACE(kTrCta, 1);
       ptx::tc_fence_after();
+
+      float s[kBlockN];
 #pragma unroll
-      for (int cc = 0; cc < D / 16; ++cc) {
-        uint32_t u[16];
-        ptx::tmem_ld16(tO + cc * 16, u);
-        ptx::tmem_wait_ld();
+      for (int cc = 0; cc < kBlockN / 32; ++cc) {
+        uint32_t u[32];
+        ptx::tmem_ld32(tS + cc * 32, u);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-        ptx::tmem_st16(tO + cc * 16, u);
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
       }
-      ptx::tmem_wait_st();
-    }
+      ptx::tmem_wait_ld();
+      // S_t is in registers: the S issuer may overwrite it with the next tile.
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::bSEmpty + t));
+      if (r == 0) DIT_TRACE(kTrSmLd0 + 5 * t, g);
 
-    // P = 2^(c*s - m), two elements per packed FMA.
-    const uint64_t c2 = ptx::f2pack(c, c);
-    const uint64_t nm2 = ptx::f2pack(-m, -m);
+      const int valid = p.n_kv - j * kBlockN;
+      if (valid < kBlockN) {
 #pragma unroll
-    for (int i = 0; i < kBlockN; i += 2) {
-      float x0, x1;
-      ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[i], s[i + 1]), c2, nm2), x0, x1);
-      s[i] = ptx::ex2_approx(x0);
-      s[i + 1] = ptx::ex2_approx(x1);
-    }
-    if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, j);
-
-    // The P_t buffer is free once PV_t(j-1) has read it.
-    if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (j - 1) & 1))) break;
-
-    // Pack P to bf16, store it (row r -> two 128-byte-swizzled K-major regions: keys 0-63,
-    // 64-127), and accumulate both row sums in independent chains.
-    uint64_t acc_l[4];
-    float acc_lp[8];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) acc_l[g] = 0;
-#pragma unroll
-    for (int g = 0; g < 8; ++g) acc_lp[g] = 0.f;
-#pragma unroll
-    for (int ch = 0; ch < kBlockN / 8; ++ch) {
-      uint32_t w[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float p0 = s[8 * ch + 2 * g], p1 = s[8 * ch + 2 * g + 1];
-        w[g] = ptx::pack_bf16x2(p0, p1);
-        acc_l[g] = ptx::fadd2(acc_l[g], ptx::f2pack(p0, p1));
-        add_bf16x2(acc_lp[2 * g], acc_lp[2 * g + 1], w[g]);
+        for (int i = 0; i < kBlockN; ++i)
+          if (i >= valid) s[i] = -INFINITY;
       }
-      const uint32_t addr =
-          sP + (ch / 8) * L::kRegion + r * 128 + ((((ch % 8) ^ (r & 7))) << 4);
-      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                   "r"(w[2]), "r"(w[3])
-                   : "memory");
-    }
-    ptx::fence_proxy_async_smem();
-    ptx::tc_fence_before();
-    ptx::mbar_arrive(bar(L::bPFull + t));
-    if (r == 0) DIT_TRACE(kTrSmArrive0 + 5 * t, j);
-    {
-      const uint64_t sl = ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
-      float a0, a1;
-      ptx::f2unpack(sl, a0, a1);
-      l += a0 + a1;
-      lp += ((acc_lp[0] + acc_lp[1]) + (acc_lp[2] + acc_lp[3])) +
-            ((acc_lp[4] + acc_lp[5]) + (acc_lp[6] + acc_lp[7]));
-    }
-  }
-  if (ok) ok = wait(L::bPVDone + t, (n_tiles - 1) & 1);
-  if (!ok) {
-    raise_abort(p, abort_flag);
-    return;
-  }
-  ptx::tc_fence_after();
-  if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2);
+      // Tile row max: 8 independent 3-input max chains, then a short tree.
+      float mx;
+      {
+        float a[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          a[q] = ptx::fmax3(s[16 * q], s[16 * q + 1], s[16 * q + 2]);
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) a[q] = ptx::fmax3(a[q], s[16 * q + i], s[16 * q + i + 1]);
+          a[q] = fmaxf(a[q], s[16 * q + 15]);
+        }
+        mx = ptx::fmax3(ptx::fmax3(a[0], a[1], a[2]), ptx::fmax3(a[3], a[4], a[5]),
+                        fmaxf(a[6], a[7]));
+      }
+      if (r == 0) DIT_TRACE(kTrSmMax0 + 5 * t, g);
+      const float m_tile = mx * c;
+      const bool raise = m_tile > m + kRescaleLog2;  // always true on an item's first tile
+      float alpha = 1.f;
+      if (raise) {
+        alpha = ptx::ex2_approx(m - m_tile);  // 0 on the first tile (m = -inf)
+        m = m_tile;
+      }
+      l *= alpha;
+      lp *= alpha;
+      bool pv_prev_done = (j == 0);  // the epilogue of the previous item waited for it
+      if (j > 0 && __any_sync(0xffffffffu, raise)) {
+        // O_t may only be touched once PV_t(g-1) has landed.
+        if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+        pv_prev_done = true;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) {
+          uint32_t u[16];
+          ptx::tmem_ld16(tO + cc * 16, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          ptx::tmem_st16(tO + cc * 16, u);
+        }
+        ptx::tmem_wait_st();
+      }
 
-  const int row = q_row0 + t * kBlockM + r;
-  const bool store = row < p.n_q;
-  // O is normalised by the sum of the rounded weights it was built from, so the weights
-  // sum to one; the LSE uses the unrounded sum.
-  const float inv_l = 1.f / lp;
-  // Stage the normalised O tile in shared memory as 128-byte-wide swizzled boxes (the
-  // P_t buffer, then Q_t: both are free once the tile's last MMAs have completed) and
-  // write it with TMA stores; rows past n_q are clipped by the tensor map.
-  constexpr int kEs = kOutF32 ? 4 : 2;
-  constexpr int kBoxCols = 128 / kEs;  // elements per 128-byte box row
-  constexpr int kBoxes = D / kBoxCols;
-  const uint32_t sQt = sbase + (t ? L::kQ1 : L::kQ0);
-  auto box_base = [&](int b) { return (b < 2 ? sP : sQt) + (b & 1) * L::kRegion; };
-  const uint32_t sw = static_cast<uint32_t>(r & 7);
+      // P = 2^(c*s - m), two elements per packed FMA.
+      const uint64_t c2 = ptx::f2pack(c, c);
+      const uint64_t nm2 = ptx::f2pack(-m, -m);
 #pragma unroll
-  for (int cc = 0; cc < D / 32; ++cc) {
-    uint32_t u[32];
-    ptx::tmem_ld32(tO + cc * 32, u);
-    ptx::tmem_wait_ld();
-    if constexpr (kOutF32) {
-      const uint32_t rowp = box_base(cc) + r * 128;
+      for (int i = 0; i < kBlockN; i += 2) {
+        float x0, x1;
+        ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[i], s[i + 1]), c2, nm2), x0, x1);
+        s[i] = ptx::ex2_approx(x0);
+        s[i + 1] = ptx::ex2_approx(x1);
+      }
+      if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, g);
+
+      // The P_t buffer is free once PV_t(g-1) has read it.
+      if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+
+      // Pack P to bf16, store it (row r -> two 128-byte-swizzled K-major regions: keys
+      // 0-63, 64-127), and accumulate both row sums in independent chains.
+      uint64_t acc_l[4];
+      float acc_lp[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = rowp + ((static_cast<uint32_t>(c) ^ sw) << 4);
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                     "f"(__uint_as_float(u[4 * c + 0]) * inv_l),
-                     "f"(__uint_as_float(u[4 * c + 1]) * inv_l),
-                     "f"(__uint_as_float(u[4 * c + 2]) * inv_l),
-                     "f"(__uint_as_float(u[4 * c + 3]) * inv_l)
+      for (int q = 0; q < 4; ++q) acc_l[q] = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc_lp[q] = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kBlockN / 8; ++ch) {
+        uint32_t wv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float p0 = s[8 * ch + 2 * q], p1 = s[8 * ch + 2 * q + 1];
+          wv[q] = ptx::pack_bf16x2(p0, p1);
+          acc_l[q] = ptx::fadd2(acc_l[q], ptx::f2pack(p0, p1));
+          add_bf16x2(acc_lp[2 * q], acc_lp[2 * q + 1], wv[q]);
+        }
+        const uint32_t addr = sP + (ch / 8) * L::kRegion + r * 128 +
+                              ((static_cast<uint32_t>(ch % 8) ^ sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]),
+                     "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
                      : "memory");
       }
-    } else {
-      const uint32_t rowp = box_base(cc / 2) + r * 128;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c = static_cast<uint32_t>((cc % 2) * 4 + i);
-        const uint32_t addr = rowp + ((c ^ sw) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 0]) * inv_l,
-                                          __uint_as_float(u[8 * i + 1]) * inv_l)),
-                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l,
-                                          __uint_as_float(u[8 * i + 3]) * inv_l)),
-                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l,
-                                          __uint_as_float(u[8 * i + 5]) * inv_l)),
-                     "r"(ptx::pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l,
-                                          __uint_as_float(u[8 * i + 7]) * inv_l))
-                     : "memory");
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(L::bPFull + t));
+      if (r == 0) DIT_TRACE(kTrSmArrive0 + 5 * t, g);
+      {
+        const uint64_t sl =
+            ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
+        float a0, a1;
+        ptx::f2unpack(sl, a0, a1);
+        l += a0 + a1;
+        lp += ((acc_lp[0] + acc_lp[1]) + (acc_lp[2] + acc_lp[3])) +
+              ((acc_lp[4] + acc_lp[5]) + (acc_lp[6] + acc_lp[7]));
       }
     }
-  }
-  ptx::fence_proxy_async_smem();
-  ptx::named_barrier(1 + t, kBlockM);
-  if (r == 0 && q_row0 + t * kBlockM < p.n_q) {  // a tile wholly past n_q stores nothing
+    if (!ok) break;
+
+    // ------------------------------------------------------------------ epilogue
+    if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+    ptx::tc_fence_after();
+    if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2 + 2 * li);
+
+    // O is normalised by the sum of the rounded weights it was built from, so the
+    // weights sum to one; the LSE uses the unrounded sum.
+    const float inv_l = 1.f / lp;
+    // The normalised O tile leaves through P_t (free: this warpgroup wrote it last and
+    // PV_t has read it) as 128-byte-wide swizzled boxes written by TMA stores, two
+    // 16 KB boxes per round; rows past n_q are clipped by the tensor map.
+    constexpr int kEs = kOutF32 ? 4 : 2;
+    constexpr int kBoxCols = 128 / kEs;            // elements per 128-byte box row
+    constexpr int kBoxes = D / kBoxCols;           // boxes per O tile
+    constexpr int kRounds = (kBoxes + 1) / 2;      // P_t holds two boxes
+    constexpr int kColsPerRound = 2 * kBoxCols < D ? 2 * kBoxCols : D;
+    const bool tile_in_range = item.q_row0 + t * kBlockM < p.n_q;
 #pragma unroll
-    for (int b = 0; b < kBoxes; ++b)
-      ptx::tma_store_3d(&p.tm_o, box_base(b), b * kBoxCols, q_row0 + t * kBlockM, bh);
-    ptx::bulk_commit_group();
-    ptx::bulk_wait_reads();  // the staging buffers may be released
+    for (int rd = 0; rd < kRounds; ++rd) {
+      uint32_t u[kColsPerRound];
+#pragma unroll
+      for (int cc = 0; cc < kColsPerRound / 32; ++cc) {
+        uint32_t v32[32];
+        ptx::tmem_ld32(tO + rd * kColsPerRound + cc * 32, v32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[cc * 32 + i] = v32[i];
+      }
+      ptx::tmem_wait_ld();
+      if (rd == kRounds - 1) {
+        // O_t has been read: the PV issuer may start the next item's O_t.
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bOEmpty + t));
+      }
+      if (rd > 0) ptx::named_barrier(1 + t, kBlockM);  // previous round's store read P_t
+#pragma unroll
+      for (int bx = 0; bx < kColsPerRound / kBoxCols; ++bx) {
+        const uint32_t rowp = sP + bx * L::kRegion + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint32_t addr = rowp + ((static_cast<uint32_t>(ch) ^ sw) << 4);
+          if constexpr (kOutF32) {
+            const int e = bx * 32 + ch * 4;
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "f"(__uint_as_float(u[e + 0]) * inv_l),
+                         "f"(__uint_as_float(u[e + 1]) * inv_l),
+                         "f"(__uint_as_float(u[e + 2]) * inv_l),
+                         "f"(__uint_as_float(u[e + 3]) * inv_l)
+                         : "memory");
+          } else {
+            const int e = bx * 64 + ch * 8;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 0]) * inv_l,
+                                              __uint_as_float(u[e + 1]) * inv_l)),
+                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 2]) * inv_l,
+                                              __uint_as_float(u[e + 3]) * inv_l)),
+                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 4]) * inv_l,
+                                              __uint_as_float(u[e + 5]) * inv_l)),
+                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 6]) * inv_l,
+                                              __uint_as_float(u[e + 7]) * inv_l))
+                         : "memory");
+          }
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::named_barrier(1 + t, kBlockM);
+      if (r == 0 && tile_in_range) {  // a tile wholly past n_q stores nothing
+#pragma unroll
+        for (int bx = 0; bx < kColsPerRound / kBoxCols; ++bx)
+          ptx::tma_store_3d(&p.tm_o, sP + bx * L::kRegion,
+                            (rd * kColsPerRound / kBoxCols + bx) * kBoxCols,
+                            item.q_row0 + t * kBlockM, item.bh);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_reads();
+      }
+    }
+    // P_t is rewritten by the next item's first tile only after every thread knows
+    // the last store has read it.
+    ptx::named_barrier(1 + t, kBlockM);
+    const int row = item.q_row0 + t * kBlockM + r;
+    if (row < p.n_q)
+      p.lse[static_cast<size_t>(item.bh) * p.n_q + row] =
+          (m + log2f(l)) * 0.69314718055994530942f;
+    if (r == 0 && t == 0) DIT_TRACE(kTrCta, 3 + 2 * li);
   }
-  if (store) p.lse[static_cast<size_t>(bh) * p.n_q + row] = (m + log2f(l)) * 0.69314718055994530942f;
-  if (r == 0 && t == 0) DIT_TRACE(kTrCta, 3);
+  if (!ok) raise_abort(p, abort_flag);
 }
 
 }  // namespace detail
@@ -609,13 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t sbase = ptx::smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int bh = blockIdx.x / p.q_pairs;
-  const int q_row0 = (blockIdx.x % p.q_pairs) * 2 * kBlockM;
   const int n_tiles = (p.n_kv + kBlockN - 1) / kBlockN;
 
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
     ptx::mbar_init(bar(L::bQFull), 1);
+    ptx::mbar_init(bar(L::bQEmpty), 1);
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(bar(L::bKFull + s), 1);
       ptx::mbar_init(bar(L::bVFull + s), 1);
@@ -626,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(L::bSEmpty + t), kBlockM);
       ptx::mbar_init(bar(L::bPFull + t), kBlockM);
       ptx::mbar_init(bar(L::bPVDone + t), 1);
+      ptx::mbar_init(bar(L::bOEmpty + t), kBlockM);
     }
     ptx::mbar_init(bar(L::bDrainS), 1);
     ptx::mbar_init(bar(L::bDrainPV), 1);
@@ -649,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (threadIdx.x == 0) DIT_TRACE(kTrCta, 0);
 
   if (warp == kLoadWarp) {
-    if (lane == 0) detail::producer<D>(p, sbase, bh, q_row0, n_tiles, abort_flag);
+    if (lane == 0) detail::producer<D>(p, sbase, n_tiles, abort_flag);
   } else if (warp == kMmaWarp) {
     if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
     __syncwarp();
@@ -657,8 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
     __syncwarp();
   } else {
-    detail::softmax_epilogue<D, kOutF32>(p, sbase, tmem, warp >> 2, warp, lane, bh, q_row0,
-                                         n_tiles, abort_flag);
+    detail::softmax_epilogue<D, kOutF32>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles,
+                                         abort_flag);
   }
 
   ptx::tc_fence_before();
@@ -667,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0) DIT_TRACE(kTrCta, 4);
+  if (threadIdx.x == 0) DIT_TRACE(kTrCta, 63);
 }
 
 }  // namespace ditattn

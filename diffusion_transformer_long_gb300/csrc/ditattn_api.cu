@@ -179,6 +179,8 @@ void dit_test_inject_stall(int enable, long long wait_limit_cycles) {
   ditattn::set_stall_injection(enable, wait_limit_cycles);
 }
 
+void dit_test_set_grid_limit(int max_ctas) { ditattn::set_grid_limit(max_ctas); }
+
 const char* dit_status_string(dit_status s) {
   switch (s) {
     case DIT_OK: return "ok";

@@ -44,4 +44,7 @@ cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st);
 // Test-only failure injection behind dit_test_inject_stall.
 void set_stall_injection(int enable, long long wait_limit_cycles);
 
+// Test-only cap on the attention kernel's persistent grid (0 = one CTA per SM).
+void set_grid_limit(int max_ctas);
+
 }  // namespace ditattn

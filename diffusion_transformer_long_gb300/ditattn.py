@@ -20,7 +20,8 @@ DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT 
 DIT_F32, DIT_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_chunk_fwd", "dit_attn_lse_merge", "dit_attn_check",
-                    "dit_test_inject_stall", "dit_status_string", "dit_version")
+                    "dit_test_inject_stall", "dit_test_set_grid_limit", "dit_status_string",
+                    "dit_version")
 
 _lib = None
 
@@ -55,6 +56,8 @@ def lib() -> ctypes.CDLL:
         L.dit_attn_check.argtypes = [P]
         L.dit_test_inject_stall.restype = None
         L.dit_test_inject_stall.argtypes = [I, LL]
+        L.dit_test_set_grid_limit.restype = None
+        L.dit_test_set_grid_limit.argtypes = [I]
         L.dit_status_string.restype = ctypes.c_char_p
         L.dit_status_string.argtypes = [I]
         L.dit_version.restype = I
@@ -194,6 +197,11 @@ def check(device=None, stream=None):
 def inject_stall(enable: bool, wait_limit_cycles: int = 0):
     """TEST ONLY: make later attention launches time out on their first K/V wait (see header)."""
     lib().dit_test_inject_stall(1 if enable else 0, int(wait_limit_cycles))
+
+
+def set_grid_limit(max_ctas: int):
+    """TEST ONLY: cap the persistent attention grid (0 restores one CTA per SM)."""
+    lib().dit_test_set_grid_limit(int(max_ctas))
 
 
 def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,

@@ -121,6 +121,14 @@ dit_status dit_attn_check(dit_stream stream);
  */
 void dit_test_inject_stall(int enable, long long wait_limit_cycles);
 
+/*
+ * TEST ONLY: caps the number of CTAs of the persistent attention kernel
+ * (normally one per SM; max_ctas <= 0 restores that).  With a small cap every
+ * CTA walks many work items, which exercises the cross-item pipeline on small
+ * inputs.  Affects later launches from this process; results do not change.
+ */
+void dit_test_set_grid_limit(int max_ctas);
+
 /* Static, human-readable name of a status code. */
 const char* dit_status_string(dit_status s);
 

@@ -336,3 +336,25 @@ def test_device_validation_errors():
     st = L.dit_attn_fwd(da._ptr(q), da._ptr(k), da._ptr(v), da._ptr(q), da._ptr(lse), 1, 1, 64,
                         128, 0.1, 0, None)
     assert st == da.DIT_ERR_INVALID_ARG  # output aliases an input
+
+
+@pytest.mark.parametrize("limit", [1, 3])
+def test_persistent_grid_many_items_per_cta(limit):
+    """A capped persistent grid makes every CTA walk many (head, Q-pair) work items, carrying
+    barrier phases, Q refills and O hand-offs across items; results must not change."""
+    da.set_grid_limit(limit)
+    try:
+        for D in (64, 128):
+            q, k, v = rand_qkv(2, 3, 700, D, seed=11 + D, scale=1.3)
+            scale = 1 / math.sqrt(D)
+            o_ref, lse_ref = oracle.attention(q, k, v, scale)
+            qd, kd, vd = to_dev(q, k, v)
+            o, lse = da.attn_fwd(qd, kd, vd, scale=scale)
+            ob, lb = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=torch.bfloat16)
+            oc, lc = da.chunk_attention(qd, kd, vd, (1, 127, 128, 129, 315), scale=scale)
+            da.check()
+            assert_parity(o, lse, o_ref, lse_ref, f"grid={limit} D={D} fused")
+            assert_parity(ob, lb, o_ref, lse_ref, f"grid={limit} D={D} bf16", bf16_out=True)
+            assert_parity(oc, lc, o_ref, lse_ref, f"grid={limit} D={D} chunks")
+    finally:
+        da.set_grid_limit(0)
