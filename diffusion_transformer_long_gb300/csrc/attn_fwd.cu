@@ -67,25 +67,6 @@ bool encode_bhnd(CUtensorMap* m, const void* base, int d, int rows, int heads,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over the output (d, rows, heads), fp32 or bf16, with 128-byte x 128-row boxes
-// and 128-byte swizzle, used for TMA stores of the normalised O tile.
-bool encode_out(CUtensorMap* m, void* base, int d, int rows, int heads, bool f32) {
-  EncodeTiledFn fn = encoder();
-  if (!fn) return false;
-  const int es = f32 ? 4 : 2;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
-                              static_cast<cuuint64_t>(heads)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
-                                 static_cast<cuuint64_t>(d) * es * static_cast<cuuint64_t>(rows)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kBlockM),
-                             1};
-  const cuuint32_t elem_strides[3] = {1, 1, 1};
-  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
-            dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int D, bool kF32>
 cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
   constexpr int kSmem = AttnSmem<D>::kBytes;
@@ -108,9 +89,11 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   AttnParams prm;
   if (!encode_bhnd(&prm.tm_q, a.q, a.d, a.n_q, a.bh, a.q_head_stride) ||
       !encode_bhnd(&prm.tm_k, a.k, a.d, a.n_kv, a.bh, a.kv_head_stride) ||
-      !encode_bhnd(&prm.tm_v, a.v, a.d, a.n_kv, a.bh, a.kv_head_stride) ||
-      !encode_out(&prm.tm_o, a.out, a.d, a.n_q, a.bh, a.out_f32))
+      !encode_bhnd(&prm.tm_v, a.v, a.d, a.n_kv, a.bh, a.kv_head_stride))
     return cudaErrorInvalidValue;
+  prm.out_f32 = a.out_f32 ? static_cast<float*>(a.out) : nullptr;
+  prm.out_bf16 = a.out_f32 ? nullptr : static_cast<__nv_bfloat16*>(a.out);
+  prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) % 32) == 0 ? 1 : 0;
   prm.lse = a.lse;
   prm.status = a.status;
   prm.n_q = a.n_q;

@@ -15,19 +15,20 @@
 // any moment share a head's K/V in L2).  Every barrier's phase count runs on across
 // items, so the next item's Q load and first S MMAs overlap this item's epilogue.
 //
-// CTA organisation (352 threads):
-//   warps 0-3  softmax + epilogue for Q tile 0   (thread = query row = TMEM lane)
-//   warps 4-7  softmax + epilogue for Q tile 1
-//   warp  8    TMA producer (Q per item, then K/V tiles through a 3-slot ring)
-//   warp  9    TMEM allocator + single-thread issuer of S = Q K^T
-//   warp 10    single-thread issuer of O += P V
+// CTA organisation (512 threads, four warpgroups):
+//   warps 0-3   softmax for Q tile 0   (thread = query row = TMEM lane)
+//   warps 4-7   softmax for Q tile 1
+//   warp  8     TMA producer (Q per item, then K/V tiles through a 3-slot ring)
+//   warp  9     TMEM allocator + single-thread issuer of S = Q K^T
+//   warp 10     single-thread issuer of O += P V       (warp 11 idle)
+//   warps 12-15 epilogue: O_t out of TMEM, normalised, stored; both Q tiles
 // Two issuers keep the tensor pipe fed: its queue is about one instruction deep,
 // and a barrier wait stalls the waiting thread for longer than one MMA, so while
 // one issuer waits the other issues.
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, fp32, lane = query row.
 // Shared memory: Q0, Q1, P0, P1 (bf16 probabilities, written by the softmax
-// warps in the 128-byte-swizzled K-major layout the MMA reads; P_t also stages
-// the O tile for its TMA store) and the K/V ring.
+// warps in the 128-byte-swizzled K-major layout the MMA reads), the K/V ring and
+// the per-row normalisers handed from the softmax to the epilogue.
 //
 // Pipeline.  A softmax warpgroup releases its S buffer (S_EMPTY) as soon as
 // the scores are in registers, so the S issuer computes S_t(g+1) = Q_t K^T while
@@ -35,8 +36,9 @@
 // tile the moment it has published P_t(g) (P_FULL).  O_t += P_t V is committed to
 // its own barrier (PV_DONE), which softmax t waits on only before it rescales O_t
 // or overwrites the P_t buffer.  Q_EMPTY (last S MMA of an item done) lets the
-// producer refill Q; O_EMPTY (epilogue has read O_t) lets the PV issuer start the
-// next item's O_t.  The K/V ring is filled in consumption order: K0, K1, V0, K2,
+// producer refill Q; at an item's end softmax t publishes 1/rowsum (EPI_READY) and
+// moves on; the epilogue warpgroup takes it (EPI_TAKEN), waits for the last PV,
+// reads O_t and releases it (O_EMPTY) to the next item's first PV.  The K/V ring is filled in consumption order: K0, K1, V0, K2,
 // V1, ... per item.
 //
 // Online softmax (base 2, scale folded into log2e): the running max m is only
@@ -84,10 +86,18 @@ enum TraceEvent {
 constexpr int kBlockM = 128;              // query rows per Q tile (two per work item)
 constexpr int kBlockN = 128;              // keys per KV tile
 constexpr int kStages = 3;                // K/V ring slots
-constexpr int kThreads = 352;
+constexpr int kThreads = 512;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;     // S = Q K^T issuer, owns the TMEM allocation
 constexpr int kPvWarp = 10;     // O += P V issuer
+constexpr int kEpiWarp0 = 12;   // warps 12-15: epilogue warpgroup
+// Register split (setmaxnreg): 512 threads launch with 128 registers each (65536);
+// softmax warpgroups grow to 176, the producer/issuer warpgroup shrinks to 72 and
+// the epilogue warpgroup to 80: 2*128*176 + 128*72 + 128*80 = 64512 <= 65536, and
+// per SM sub-partition (one warp of each warpgroup) 176+176+72+80 = 504 <= 512.
+constexpr uint32_t kRegsSoftmax = 176;
+constexpr uint32_t kRegsIssue = 72;
+constexpr uint32_t kRegsEpilogue = 80;
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
@@ -96,7 +106,9 @@ struct AttnParams {
   CUtensorMap tm_q;   // (D, n_q, bh) bf16, box (64, 128, 1), 128B swizzle
   CUtensorMap tm_k;   // (D, n_kv, bh), head stride = kv_head_stride
   CUtensorMap tm_v;
-  CUtensorMap tm_o;   // (D, n_q, bh) fp32 or bf16, box (128 bytes, 128, 1), 128B swizzle (stores)
+  float* out_f32;     // [bh, n_q, D] (fp32 output) or null
+  __nv_bfloat16* out_bf16;  // [bh, n_q, D] (bf16 output) or null
+  int out_align32;    // the output base is 32-byte aligned (full-sector stores)
   float* lse;         // [bh, n_q]
   int* status;        // device status word (timeouts)
   int n_q;
@@ -132,12 +144,15 @@ struct AttnSmem {
   static constexpr int bPFull = bSEmpty + 2;         // + tile: P_t written (128 arrivals)
   static constexpr int bPVDone = bPFull + 2;         // + tile: O_t += P_t V done (MMA commit)
   static constexpr int bOEmpty = bPVDone + 2;        // + tile: O_t read by the epilogue (128 arrivals)
-  static constexpr int bDrainS = bOEmpty + 2;        // abort drain, S issuer
+  static constexpr int bEpiReady = bOEmpty + 2;      // + tile: normaliser of an item written (128)
+  static constexpr int bEpiTaken = bEpiReady + 2;    // + tile: normaliser read by the epilogue (128)
+  static constexpr int bDrainS = bEpiTaken + 2;      // abort drain, S issuer
   static constexpr int bDrainPV = bDrainS + 1;       // abort drain, PV issuer
   static constexpr int kNumBars = bDrainPV + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kUsed = kAbort + 4;
+  static constexpr uint32_t kInvLp = (kAbort + 4 + 15) & ~15u;  // [2][128] fp32: 1 / row sum
+  static constexpr uint32_t kUsed = kInvLp + 2 * kBlockM * 4;
   static constexpr uint32_t kBytes = kUsed + 1024;   // slack for 1024-byte alignment
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -420,10 +435,10 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
       : "r"(w));
 }
 
-template <int D, bool kOutF32>
-__device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t sbase,
-                                                 uint32_t tmem, int t, int warp, int lane,
-                                                 int n_tiles, volatile int* abort_flag) {
+template <int D>
+__device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
+                                           int t, int warp, int lane, int n_tiles,
+                                           volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int quarter = warp & 3;
@@ -434,6 +449,8 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
   const uint32_t sP = sbase + (t ? L::kP1 : L::kP0);
   const uint32_t sw = static_cast<uint32_t>(r & 7);
   const float c = p.scale_log2;
+  float* inv_lp_slot = reinterpret_cast<float*>(
+      __cvta_shared_to_generic(sbase + L::kInvLp)) + t * kBlockM + r;
   // Warp-uniform bounded wait.
   auto wait = [&](int b, uint32_t parity) {
     const bool ok = wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
@@ -498,7 +515,7 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
       }
       l *= alpha;
       lp *= alpha;
-      bool pv_prev_done = (j == 0);  // the epilogue of the previous item waited for it
+      bool pv_prev_done = (g == 0);  // no earlier PV has read P_t
       if (j > 0 && __any_sync(0xffffffffu, raise)) {
         // O_t may only be touched once PV_t(g-1) has landed.
         if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
@@ -571,89 +588,113 @@ __device__ __forceinline__ void softmax_epilogue(const AttnParams& p, uint32_t s
     }
     if (!ok) break;
 
-    // ------------------------------------------------------------------ epilogue
-    if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
-    ptx::tc_fence_after();
-    if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2 + 2 * li);
-
-    // O is normalised by the sum of the rounded weights it was built from, so the
-    // weights sum to one; the LSE uses the unrounded sum.
-    const float inv_l = 1.f / lp;
-    // The normalised O tile leaves through P_t (free: this warpgroup wrote it last and
-    // PV_t has read it) as 128-byte-wide swizzled boxes written by TMA stores, two
-    // 16 KB boxes per round; rows past n_q are clipped by the tensor map.
-    constexpr int kEs = kOutF32 ? 4 : 2;
-    constexpr int kBoxCols = 128 / kEs;            // elements per 128-byte box row
-    constexpr int kBoxes = D / kBoxCols;           // boxes per O tile
-    constexpr int kRounds = (kBoxes + 1) / 2;      // P_t holds two boxes
-    constexpr int kColsPerRound = 2 * kBoxCols < D ? 2 * kBoxCols : D;
-    const bool tile_in_range = item.q_row0 + t * kBlockM < p.n_q;
-#pragma unroll
-    for (int rd = 0; rd < kRounds; ++rd) {
-      uint32_t u[kColsPerRound];
-#pragma unroll
-      for (int cc = 0; cc < kColsPerRound / 32; ++cc) {
-        uint32_t v32[32];
-        ptx::tmem_ld32(tO + rd * kColsPerRound + cc * 32, v32);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) u[cc * 32 + i] = v32[i];
-      }
-      ptx::tmem_wait_ld();
-      if (rd == kRounds - 1) {
-        // O_t has been read: the PV issuer may start the next item's O_t.
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::bOEmpty + t));
-      }
-      if (rd > 0) ptx::named_barrier(1 + t, kBlockM);  // previous round's store read P_t
-#pragma unroll
-      for (int bx = 0; bx < kColsPerRound / kBoxCols; ++bx) {
-        const uint32_t rowp = sP + bx * L::kRegion + r * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint32_t addr = rowp + ((static_cast<uint32_t>(ch) ^ sw) << 4);
-          if constexpr (kOutF32) {
-            const int e = bx * 32 + ch * 4;
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "f"(__uint_as_float(u[e + 0]) * inv_l),
-                         "f"(__uint_as_float(u[e + 1]) * inv_l),
-                         "f"(__uint_as_float(u[e + 2]) * inv_l),
-                         "f"(__uint_as_float(u[e + 3]) * inv_l)
-                         : "memory");
-          } else {
-            const int e = bx * 64 + ch * 8;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 0]) * inv_l,
-                                              __uint_as_float(u[e + 1]) * inv_l)),
-                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 2]) * inv_l,
-                                              __uint_as_float(u[e + 3]) * inv_l)),
-                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 4]) * inv_l,
-                                              __uint_as_float(u[e + 5]) * inv_l)),
-                         "r"(ptx::pack_bf16x2(__uint_as_float(u[e + 6]) * inv_l,
-                                              __uint_as_float(u[e + 7]) * inv_l))
-                         : "memory");
-          }
-        }
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::named_barrier(1 + t, kBlockM);
-      if (r == 0 && tile_in_range) {  // a tile wholly past n_q stores nothing
-#pragma unroll
-        for (int bx = 0; bx < kColsPerRound / kBoxCols; ++bx)
-          ptx::tma_store_3d(&p.tm_o, sP + bx * L::kRegion,
-                            (rd * kColsPerRound / kBoxCols + bx) * kBoxCols,
-                            item.q_row0 + t * kBlockM, item.bh);
-        ptx::bulk_commit_group();
-        ptx::bulk_wait_reads();
-      }
-    }
-    // P_t is rewritten by the next item's first tile only after every thread knows
-    // the last store has read it.
-    ptx::named_barrier(1 + t, kBlockM);
+    // Hand the row's normaliser to the epilogue warpgroup and write the LSE.  O is
+    // normalised by the sum of the rounded weights it was built from, so the weights
+    // sum to one; the LSE uses the unrounded sum.  The slot is reused once the
+    // epilogue has taken the previous item's value.
+    if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
+    *inv_lp_slot = 1.f / lp;
+    ptx::mbar_arrive(bar(L::bEpiReady + t));
     const int row = item.q_row0 + t * kBlockM + r;
     if (row < p.n_q)
       p.lse[static_cast<size_t>(item.bh) * p.n_q + row] =
           (m + log2f(l)) * 0.69314718055994530942f;
-    if (r == 0 && t == 0) DIT_TRACE(kTrCta, 3 + 2 * li);
+  }
+  if (!ok) raise_abort(p, abort_flag);
+}
+
+// Epilogue warpgroup (warps 12-15): for each work item and Q tile t, waits for the
+// softmax's normaliser and the tile's last PV, reads O_t out of tensor memory (then
+// releases it to the next item's PV), scales it and stores it.  Off the softmax's
+// critical path: the softmax warpgroups go straight on to the next item.
+template <int D, bool kOutF32>
+__device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
+                                            int warp, int lane, int n_tiles,
+                                            volatile int* abort_flag) {
+  using L = AttnSmem<D>;
+  auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;  // row in the Q tile == TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const float* inv_lp = reinterpret_cast<const float*>(__cvta_shared_to_generic(sbase + L::kInvLp));
+  auto wait = [&](int b, uint32_t parity) {
+    const bool ok = wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
+    return __all_sync(0xffffffffu, ok);
+  };
+
+  int li = 0;
+  bool ok = true;
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
+    const Item item = item_of(p, w);
+    const int g_last = (li + 1) * n_tiles - 1;  // CTA-global index of the item's last tile
+    for (int t = 0; t < 2; ++t) {
+      if (!(ok = wait(L::bEpiReady + t, li & 1))) break;
+      const float inv_l = inv_lp[t * kBlockM + r];
+      ptx::mbar_arrive(bar(L::bEpiTaken + t));
+      if (!(ok = wait(L::bPVDone + t, g_last & 1))) break;
+      ptx::tc_fence_after();
+      if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2 + 2 * li);
+      const uint32_t tO = tmem + 2 * kBlockN + t * D + lane_off;
+      const int row = item.q_row0 + t * kBlockM + r;
+      const bool store = row < p.n_q;
+      const size_t out_row = (static_cast<size_t>(item.bh) * p.n_q + row) * D;
+      // Two 32-column chunks per TMEM read; O_t is released as soon as the last chunk is
+      // in registers, before its stores.  Rows are written with 32-byte stores (full
+      // sectors) when the output is 32-byte aligned, else 16-byte stores.
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t u[64];
+        {
+          uint32_t a[32], b[32];
+          ptx::tmem_ld32(tO + half * 64, a);
+          ptx::tmem_ld32(tO + half * 64 + 32, b);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            u[i] = a[i];
+            u[32 + i] = b[i];
+          }
+        }
+        if (half == D / 64 - 1) {
+          // O_t has been read: the PV issuer may start the next item's O_t.
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bOEmpty + t));
+        }
+        if (!store) continue;
+        auto v = [&](int i) { return __uint_as_float(u[i]) * inv_l; };
+        if constexpr (kOutF32) {
+          float* dst = p.out_f32 + out_row + half * 64;
+          if (p.out_align32) {
+#pragma unroll
+            for (int i = 0; i < 64; i += 8)
+              asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + i),
+                           "f"(v(i)), "f"(v(i + 1)), "f"(v(i + 2)), "f"(v(i + 3)), "f"(v(i + 4)),
+                           "f"(v(i + 5)), "f"(v(i + 6)), "f"(v(i + 7))
+                           : "memory");
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; i += 4)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(v(i), v(i + 1), v(i + 2), v(i + 3));
+          }
+        } else {
+          __nv_bfloat16* dst = p.out_bf16 + out_row + half * 64;
+          auto w = [&](int i) { return ptx::pack_bf16x2(v(2 * i), v(2 * i + 1)); };
+          if (p.out_align32) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
+              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 2 * i),
+                           "r"(w(i)), "r"(w(i + 1)), "r"(w(i + 2)), "r"(w(i + 3)), "r"(w(i + 4)),
+                           "r"(w(i + 5)), "r"(w(i + 6)), "r"(w(i + 7))
+                           : "memory");
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w(i), w(i + 1), w(i + 2), w(i + 3));
+          }
+        }
+      }
+      if (r == 0 && t == 0) DIT_TRACE(kTrCta, 3 + 2 * li);
+    }
   }
   if (!ok) raise_abort(p, abort_flag);
 }
@@ -686,6 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(L::bPFull + t), kBlockM);
       ptx::mbar_init(bar(L::bPVDone + t), 1);
       ptx::mbar_init(bar(L::bOEmpty + t), kBlockM);
+      ptx::mbar_init(bar(L::bEpiReady + t), kBlockM);
+      ptx::mbar_init(bar(L::bEpiTaken + t), kBlockM);
     }
     ptx::mbar_init(bar(L::bDrainS), 1);
     ptx::mbar_init(bar(L::bDrainPV), 1);
@@ -696,7 +739,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::tma_prefetch_desc(&p.tm_q);
     ptx::tma_prefetch_desc(&p.tm_k);
     ptx::tma_prefetch_desc(&p.tm_v);
-    ptx::tma_prefetch_desc(&p.tm_o);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(sbase + L::kTmemSlot, 512);
@@ -708,17 +750,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   if (threadIdx.x == 0) DIT_TRACE(kTrCta, 0);
 
-  if (warp == kLoadWarp) {
-    if (lane == 0) detail::producer<D>(p, sbase, n_tiles, abort_flag);
-  } else if (warp == kMmaWarp) {
-    if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
-    __syncwarp();
-  } else if (warp == kPvWarp) {
-    if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+  if (warp < kLoadWarp) {
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    detail::softmax_wg<D>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles, abort_flag);
+  } else if (warp < kEpiWarp0) {
+    ptx::setmaxnreg_dec<kRegsIssue>();
+    if (warp == kLoadWarp) {
+      if (lane == 0) detail::producer<D>(p, sbase, n_tiles, abort_flag);
+    } else if (warp == kMmaWarp) {
+      if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+    } else if (warp == kPvWarp) {
+      if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+    }
     __syncwarp();
   } else {
-    detail::softmax_epilogue<D, kOutF32>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles,
-                                         abort_flag);
+    ptx::setmaxnreg_dec<kRegsEpilogue>();
+    detail::epilogue_wg<D, kOutF32>(p, sbase, tmem, warp, lane, n_tiles, abort_flag);
   }
 
   ptx::tc_fence_before();

@@ -274,6 +274,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register reallocation; every warp of the warpgroup executes it.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---------------------------------------------------------------- packed fp32
 // Blackwell executes these on pairs of fp32 registers in one instruction.
 __device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
