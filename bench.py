@@ -331,6 +331,29 @@ def run_gpu(args):
     step_flops = 2 * w.flops  # the fused pass and the chunked pass each compute the attention
     value = step_flops * world / (ms_step * 1e-3) / 1e12
 
+    # ---- chunk path with bf16 partials (a stated variant; timed outside the step) ----
+    parts16 = torch.empty((p, B, H, N, D), device=dev, dtype=torch.bfloat16)
+
+    def chunk_bf16():
+        for c, (s, n) in enumerate(zip(starts, w.chunks)):
+            da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=parts16[c], lse=lses[c],
+                              scale=w.scale)
+        da.attn_lse_merge(parts16, lses, out=out_c, lse=lse_c)
+
+    for _ in range(args.warmup):
+        chunk_bf16()
+    torch.cuda.synchronize(dev)
+    b0, b1 = ev(), ev()
+    b0.record(stream)
+    n16 = max(3, args.steps // 3)
+    for _ in range(n16):
+        chunk_bf16()
+    b1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    chunk16_ms = max_over_ranks(dist, b0.elapsed_time(b1) / n16)
+    del parts16
+
     # ---- end to end through the public API with host buffers ----
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     o1_h = torch.empty(out_f.shape, dtype=torch.float32, pin_memory=True)
@@ -401,6 +424,9 @@ def run_gpu(args):
                                 "ratio_to_fused": chunk_ms / fused_ms,
                                 "merge_ms": merge_ms, "merge_gbs": merge_gbs,
                                 "merge_frac_of_hbm": merge_gbs / hbm},
+                "chunk_merge_bf16_partials": {"ms": chunk16_ms,
+                                              "tflops": w.flops / (chunk16_ms * 1e-3) / 1e12,
+                                              "ratio_to_fused": chunk16_ms / fused_ms},
                 "fused_vs_chunk_max_abs": diff,
             },
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,fp32>",

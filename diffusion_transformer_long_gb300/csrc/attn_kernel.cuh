@@ -99,6 +99,10 @@ constexpr uint32_t kRegsSoftmax = 176;
 constexpr uint32_t kRegsIssue = 72;
 constexpr uint32_t kRegsEpilogue = 80;
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
+#ifndef DITATTN_STORE_PACE_NS
+#define DITATTN_STORE_PACE_NS 0
+#endif
+constexpr unsigned kStorePaceNs = DITATTN_STORE_PACE_NS;  // gap between paced O stores (0: none)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
 
@@ -640,7 +644,11 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
       const size_t out_row = (static_cast<size_t>(item.bh) * p.n_q + row) * D;
       // Two 32-column chunks per TMEM read; O_t is released as soon as the last chunk is
       // in registers, before its stores.  Rows are written with 32-byte stores (full
-      // sectors) when the output is 32-byte aligned, else 16-byte stores.
+      // sectors) when the output is 32-byte aligned, else 16-byte stores.  Each warp store
+      // touches 32 rows (32 sectors); a burst of them can hold up the softmax's shared-
+      // memory P writes at the start of the next item, so the stores issued after O_t is
+      // released can be paced kStorePaceNs apart (off by default: on the Wan2.2 workload
+      // pacing trades ~1 % of the fused pass for ~1 % of the chunk path).
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
         uint32_t u[64];
@@ -662,34 +670,45 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
         }
         if (!store) continue;
         auto v = [&](int i) { return __uint_as_float(u[i]) * inv_l; };
+        auto pace = [&]() {
+          if (kStorePaceNs > 0 && half == D / 64 - 1) __nanosleep(kStorePaceNs);
+        };
         if constexpr (kOutF32) {
           float* dst = p.out_f32 + out_row + half * 64;
           if (p.out_align32) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 8)
+            for (int i = 0; i < 64; i += 8) {
+              pace();
               asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + i),
                            "f"(v(i)), "f"(v(i + 1)), "f"(v(i + 2)), "f"(v(i + 3)), "f"(v(i + 4)),
                            "f"(v(i + 5)), "f"(v(i + 6)), "f"(v(i + 7))
                            : "memory");
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 64; i += 4)
+            for (int i = 0; i < 64; i += 4) {
+              if (i % 8 == 0) pace();
               *reinterpret_cast<float4*>(dst + i) = make_float4(v(i), v(i + 1), v(i + 2), v(i + 3));
+            }
           }
         } else {
           __nv_bfloat16* dst = p.out_bf16 + out_row + half * 64;
           auto w = [&](int i) { return ptx::pack_bf16x2(v(2 * i), v(2 * i + 1)); };
           if (p.out_align32) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8)
+            for (int i = 0; i < 32; i += 8) {
+              pace();
               asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 2 * i),
                            "r"(w(i)), "r"(w(i + 1)), "r"(w(i + 2)), "r"(w(i + 3)), "r"(w(i + 4)),
                            "r"(w(i + 5)), "r"(w(i + 6)), "r"(w(i + 7))
                            : "memory");
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
+            for (int i = 0; i < 32; i += 4) {
+              if (i % 8 == 0) pace();
               *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w(i), w(i + 1), w(i + 2), w(i + 3));
+            }
           }
         }
       }
