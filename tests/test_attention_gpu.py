@@ -358,3 +358,25 @@ def test_persistent_grid_many_items_per_cta(limit):
             assert_parity(oc, lc, o_ref, lse_ref, f"grid={limit} D={D} chunks")
     finally:
         da.set_grid_limit(0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_output_16_byte_aligned_not_32(dtype):
+    """The epilogue writes 32-byte vectors when the output is 32-byte aligned and falls back to
+    16-byte vectors otherwise; both must give the same result and touch nothing outside."""
+    B, H, N, D = 1, 2, 300, 128
+    q, k, v = rand_qkv(B, H, N, D, seed=21)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    n = B * H * N * D
+    shift = 16 // torch.empty((), dtype=dtype).element_size()  # 16 bytes
+    big = torch.full((n + 64,), 7.0, device=DEV, dtype=dtype)
+    out = big[shift:shift + n].view(B, H, N, D)
+    assert out.data_ptr() % 32 == 16
+    o, lse = da.attn_fwd(qd, kd, vd, out=out, scale=scale)
+    o_al, _ = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=dtype)
+    da.check()
+    assert torch.equal(o, o_al)
+    assert (big[:shift] == 7.0).all() and (big[shift + n:] == 7.0).all()
+    assert_parity(o, lse, o_ref, lse_ref, f"16B-aligned {dtype}", bf16_out=dtype == torch.bfloat16)
