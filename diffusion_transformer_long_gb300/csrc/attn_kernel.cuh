@@ -475,11 +475,14 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       if (r == 0 && t == 0 && g == 0) DIT_TRACE(kTrCta, 1);
       ptx::tc_fence_after();
 
+      // Scores into registers; the load-with-reduction form returns each 32-column
+      // chunk's max as well, so a full tile's row max costs two extra instructions.
       float s[kBlockN];
+      float cmax[kBlockN / 32];
 #pragma unroll
       for (int cc = 0; cc < kBlockN / 32; ++cc) {
         uint32_t u[32];
-        ptx::tmem_ld32(tS + cc * 32, u);
+        ptx::tmem_ld32_max(tS + cc * 32, u, cmax[cc]);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
       }
@@ -489,15 +492,14 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       ptx::mbar_arrive(bar(L::bSEmpty + t));
       if (r == 0) DIT_TRACE(kTrSmLd0 + 5 * t, g);
 
+      float mx = ptx::fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
       const int valid = p.n_kv - j * kBlockN;
       if (valid < kBlockN) {
+        // Ragged last tile: keys past n_kv (zero-filled K rows) are masked to -inf and
+        // the max is taken over the valid columns only.
 #pragma unroll
         for (int i = 0; i < kBlockN; ++i)
           if (i >= valid) s[i] = -INFINITY;
-      }
-      // Tile row max: 8 independent 3-input max chains, then a short tree.
-      float mx;
-      {
         float a[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {

@@ -232,6 +232,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
+// Same as tmem_ld32 and also returns, per thread, the maximum of the 32 loaded
+// values as fp32 (the load-with-reduction form of sm_103a).
+__device__ __forceinline__ void tmem_ld32_max(uint32_t taddr, uint32_t (&r)[32], float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : DITATTN_R8(0), DITATTN_R8(8), DITATTN_R8(16), DITATTN_R8(24), "=f"(mx)
+      : "r"(taddr));
+}
+
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
