@@ -354,6 +354,48 @@ def run_gpu(args):
     chunk16_ms = max_over_ranks(dist, b0.elapsed_time(b1) / n16)
     del parts16
 
+    # ---- hop-by-hop ring: each chunk pass merges into the running (O, lse) itself ----
+    # The first hop writes the running state (dit_attn_chunk_fwd, fp32), the other p-1 fold
+    # their chunk in (dit_attn_chunk_fwd_accumulate): no stacked partials, no merge pass.
+    def ring():
+        for c, (s, n) in enumerate(zip(starts, w.chunks)):
+            kc, vc = k[:, :, s:s + n], v[:, :, s:s + n]
+            if c == 0:
+                da.attn_chunk_fwd(q, kc, vc, out=out_c, lse=lse_c, scale=w.scale)
+            else:
+                da.attn_chunk_fwd_accumulate(q, kc, vc, out_c, lse_c, scale=w.scale)
+
+    for _ in range(args.warmup):
+        ring()
+    torch.cuda.synchronize(dev)
+    r0, r1 = ev(), ev()
+    r0.record(stream)
+    nr = max(3, args.steps // 3)
+    for _ in range(nr):
+        ring()
+    r1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    ring_ms = max_over_ranks(dist, r0.elapsed_time(r1) / nr)
+    ring_diff = (out_f - out_c).abs().max().item()
+
+    # ---- cross-attention shape: all N queries against 512 replicated text keys ----
+    n_txt = 512
+    kx, vx = k[:, :, :n_txt], v[:, :, :n_txt]
+    for _ in range(args.warmup):
+        da.attn_chunk_fwd(q, kx, vx, out=out_c, lse=lse_c, scale=w.scale)
+    torch.cuda.synchronize(dev)
+    x0, x1 = ev(), ev()
+    x0.record(stream)
+    nx = max(5, args.steps)
+    for _ in range(nx):
+        da.attn_chunk_fwd(q, kx, vx, out=out_c, lse=lse_c, scale=w.scale)
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    cross_ms = max_over_ranks(dist, x0.elapsed_time(x1) / nx)
+    cross_flops = 4.0 * B * H * N * n_txt * D
+
     # ---- end to end through the public API with host buffers ----
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
     o1_h = torch.empty(out_f.shape, dtype=torch.float32, pin_memory=True)
@@ -427,6 +469,12 @@ def run_gpu(args):
                 "chunk_merge_bf16_partials": {"ms": chunk16_ms,
                                               "tflops": w.flops / (chunk16_ms * 1e-3) / 1e12,
                                               "ratio_to_fused": chunk16_ms / fused_ms},
+                "ring_accumulate": {"ms": ring_ms,
+                                    "tflops": w.flops / (ring_ms * 1e-3) / 1e12,
+                                    "ratio_to_fused": ring_ms / fused_ms,
+                                    "max_abs_vs_fused": ring_diff},
+                "cross_attention_512_text_keys": {"ms": cross_ms,
+                                                  "tflops": cross_flops / (cross_ms * 1e-3) / 1e12},
                 "fused_vs_chunk_max_abs": diff,
             },
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,fp32>",

@@ -67,10 +67,10 @@ bool encode_bhnd(CUtensorMap* m, const void* base, int d, int rows, int heads,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kF32>
+template <int D, bool kF32, bool kAccum = false>
 cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
   constexpr int kSmem = AttnSmem<D>::kBytes;
-  auto kern = attn_fwd_kernel<D, kF32>;
+  auto kern = attn_fwd_kernel<D, kF32, kAccum>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   // Persistent grid: one CTA per SM (shared memory and TMEM allow no more), each
@@ -104,6 +104,10 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;
   prm.stall_kv = g_stall_kv;
+  if (a.accumulate) {
+    if (!a.out_f32) return cudaErrorInvalidValue;
+    return a.d == 64 ? launch_typed<64, true, true>(prm, st) : launch_typed<128, true, true>(prm, st);
+  }
   if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
   return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);
 }

@@ -77,7 +77,7 @@ namespace ditattn {
 enum TraceEvent {
   kTrProdEmpty = 0, kTrProdIssue, kTrMmaK, kTrMmaS0, kTrMmaS1, kTrMmaV, kTrMmaP0, kTrMmaPv0,
   kTrMmaP1, kTrMmaPv1, kTrSmFull0, kTrSmLd0, kTrSmMax0, kTrSmExp0, kTrSmArrive0,
-  kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1, kTrCta
+  kTrSmFull1, kTrSmLd1, kTrSmMax1, kTrSmExp1, kTrSmArrive1, kTrCta, kTrQIssue, kTrQFull
 };
 // Per-tile events are indexed by the CTA-global tile count; kTrCta slots: 0 start,
 // 1 first S seen, then per item i: 2 + 2i epilogue start, 3 + 2i epilogue end
@@ -98,11 +98,8 @@ constexpr int kEpiWarp0 = 12;   // warps 12-15: epilogue warpgroup
 constexpr uint32_t kRegsSoftmax = 176;
 constexpr uint32_t kRegsIssue = 72;
 constexpr uint32_t kRegsEpilogue = 80;
+constexpr uint32_t kRegsEpilogueAccum = 88;  // 2*128*176 + 128*72 + 128*88 = 65536
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
-#ifndef DITATTN_STORE_PACE_NS
-#define DITATTN_STORE_PACE_NS 0
-#endif
-constexpr unsigned kStorePaceNs = DITATTN_STORE_PACE_NS;  // gap between paced O stores (0: none)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
 
@@ -255,6 +252,7 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
       for (int r = 0; r < kRegions; ++r)
         ptx::tma_load_3d(sbase + (t ? L::kQ1 : L::kQ0) + r * L::kRegion, &p.tm_q,
                          bar(L::bQFull), r * 64, item.q_row0 + t * kBlockM, item.bh);
+    DIT_TRACE(kTrQIssue, q_loads);
     ++q_loads;
     if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
 
@@ -340,6 +338,7 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
   bool ok = true;
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li, ring0 += 2 * n_tiles) {
     if (!(ok = wait(L::bQFull, li & 1))) break;
+    DIT_TRACE(kTrQFull, li);
     for (int j = 0; j < n_tiles; ++j, ++g) {
       const int sK = (ring0 + k_item(j)) % kStages;
       ok = wait(L::bKFull + sK, (kpar >> sK) & 1);
@@ -439,7 +438,7 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
       : "r"(w));
 }
 
-template <int D>
+template <int D, bool kAccum>
 __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                            int t, int warp, int lane, int n_tiles,
                                            volatile int* abort_flag) {
@@ -453,8 +452,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
   const uint32_t sP = sbase + (t ? L::kP1 : L::kP0);
   const uint32_t sw = static_cast<uint32_t>(r & 7);
   const float c = p.scale_log2;
-  float* inv_lp_slot = reinterpret_cast<float*>(
-      __cvta_shared_to_generic(sbase + L::kInvLp)) + t * kBlockM + r;
+  float* const hand = reinterpret_cast<float*>(__cvta_shared_to_generic(sbase + L::kInvLp));
   // Warp-uniform bounded wait.
   auto wait = [&](int b, uint32_t parity) {
     const bool ok = wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
@@ -594,35 +592,94 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     }
     if (!ok) break;
 
-    // Hand the row's normaliser to the epilogue warpgroup and write the LSE.  O is
+    // Hand the row's scale factors to the epilogue warpgroup and write the LSE.  O is
     // normalised by the sum of the rounded weights it was built from, so the weights
-    // sum to one; the LSE uses the unrounded sum.  The slot is reused once the
-    // epilogue has taken the previous item's value.
-    if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
-    *inv_lp_slot = 1.f / lp;
-    ptx::mbar_arrive(bar(L::bEpiReady + t));
+    // sum to one; the LSE uses the unrounded sum.
+    constexpr float kLn2 = 0.69314718055994530942f;
+    const float lse2 = m + log2f(l);  // this pass's LSE in log2 units
     const int row = item.q_row0 + t * kBlockM + r;
-    if (row < p.n_q)
-      p.lse[static_cast<size_t>(item.bh) * p.n_q + row] =
-          (m + log2f(l)) * 0.69314718055994530942f;
+    float* const lse_row = p.lse + static_cast<size_t>(item.bh) * p.n_q + row;
+    if constexpr (!kAccum) {
+      // Slot [t][r] = 1 / lp, reused once the epilogue has taken the previous item's value.
+      if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
+      hand[t * kBlockM + r] = 1.f / lp;
+      ptx::mbar_arrive(bar(L::bEpiReady + t));
+      if (row < p.n_q) *lse_row = lse2 * kLn2;
+    } else {
+      // Accumulate mode: the epilogue merges this pass into the running (O, lse); it gets
+      // (this pass's LSE in log2 units, 1 / lp) through one slot [r][2] shared by both Q
+      // tiles, filled in the order tile 0, tile 1 of each item.
+      (void)lse_row;
+      if (t == 0) {
+        if (li > 0 && !(ok = wait(L::bEpiTaken + 1, (li - 1) & 1))) break;
+      } else if (!(ok = wait(L::bEpiTaken + 0, li & 1))) {
+        break;
+      }
+      hand[2 * r] = lse2;
+      hand[2 * r + 1] = 1.f / lp;
+      ptx::mbar_arrive(bar(L::bEpiReady + t));
+    }
   }
   if (!ok) raise_abort(p, abort_flag);
+}
+
+// One butterfly stage of a warp-wide register<->lane transpose: lane bit kLaneBit and bit
+// kRegBit of the register index trade meanings (each pair of registers differing in that
+// register bit exchanges one value with the lane differing in that lane bit).
+template <int kLaneBit, int kRegBit, int N>
+__device__ __forceinline__ void swap_lane_reg_bit(uint32_t (&x)[N], int lane) {
+  const bool hi = (lane >> kLaneBit) & 1;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (i & (1 << kRegBit)) continue;
+    const int j = i | (1 << kRegBit);
+    const uint32_t send = hi ? x[i] : x[j];
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1 << kLaneBit);
+    x[i] = hi ? recv : x[i];
+    x[j] = hi ? x[j] : recv;
+  }
+}
+
+// 32 bytes to global memory: one 32-byte store when dst is 32-byte aligned, else two 16-byte ones.
+__device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uint32_t* a) {
+  if (align32) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a[0]),
+                 "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a[0]), "r"(a[1]),
+                 "r"(a[2]), "r"(a[3])
+                 : "memory");
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(static_cast<char*>(dst) + 16),
+                 "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+                 : "memory");
+  }
 }
 
 // Epilogue warpgroup (warps 12-15): for each work item and Q tile t, waits for the
 // softmax's normaliser and the tile's last PV, reads O_t out of tensor memory (then
 // releases it to the next item's PV), scales it and stores it.  Off the softmax's
 // critical path: the softmax warpgroups go straight on to the next item.
-template <int D, bool kOutF32>
+//
+// TMEM hands each thread one row.  For fp32 output two butterfly stages (warp shuffles)
+// trade lane bits 4,3 (row) with register bits 4,3 (column) of each 32-column chunk, so
+// that one warp store covers 8 rows x 128 contiguous bytes rather than 32 rows x 32
+// bytes: a quarter of the L1 wavefronts per byte, which keeps the burst of O stores at an
+// item boundary from holding up the softmax's shared-memory P writes.  bf16 rows are
+// stored from the row-per-thread layout (64 bytes per row per 32 columns), which measured
+// faster there.
+template <int D, bool kOutF32, bool kAccum>
 __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                             int warp, int lane, int n_tiles,
                                             volatile int* abort_flag) {
+  static_assert(kOutF32 || !kAccum, "the running output is fp32");
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;  // row in the Q tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-  const float* inv_lp = reinterpret_cast<const float*>(__cvta_shared_to_generic(sbase + L::kInvLp));
+  const float* hand = reinterpret_cast<const float*>(__cvta_shared_to_generic(sbase + L::kInvLp));
+  const int r_lo = lane & 7, cgrp = lane >> 3;  // fp32 store layout after the transpose
   auto wait = [&](int b, uint32_t parity) {
     const bool ok = wait_or_abort(bar(b), parity, abort_flag, p.wait_limit);
     return __all_sync(0xffffffffu, ok);
@@ -633,84 +690,147 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
     const Item item = item_of(p, w);
     const int g_last = (li + 1) * n_tiles - 1;  // CTA-global index of the item's last tile
+    const size_t head_row0 = static_cast<size_t>(item.bh) * p.n_q;
+    // Accumulate mode: this item's running LSEs (read now, long before they are needed)
+    // and its running-output rows brought into L2 while the item runs.
+    float lse_run0 = -INFINITY, lse_run1 = -INFINITY;
+    if constexpr (kAccum) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int row = item.q_row0 + t * kBlockM + r;
+        if (row < p.n_q) {
+          (t ? lse_run1 : lse_run0) = ptx::ld_global_f32(p.lse + head_row0 + row);
+#pragma unroll
+          for (int q = 0; q < D / 32; ++q) ptx::prefetch_l2(p.out_f32 + (head_row0 + row) * D + q * 32);
+        }
+      }
+    }
     for (int t = 0; t < 2; ++t) {
       if (!(ok = wait(L::bEpiReady + t, li & 1))) break;
-      const float inv_l = inv_lp[t * kBlockM + r];
-      ptx::mbar_arrive(bar(L::bEpiTaken + t));
+      // Scale of this row's O accumulator, and in accumulate mode the weight of the
+      // running output.
+      float inv_l, w_run = 0.f;
+      if constexpr (!kAccum) {
+        inv_l = hand[t * kBlockM + r];
+        ptx::mbar_arrive(bar(L::bEpiTaken + t));
+      } else {
+        const float lse2 = hand[2 * r], inv_lp = hand[2 * r + 1];
+        ptx::mbar_arrive(bar(L::bEpiTaken + t));
+        // Merge into the running (O, lse) exactly as one ring hop does:
+        //   lse' = M + ln(e^(lse_run - M) + e^(lse_c - M)),  M = max(lse_run, lse_c),
+        //   O'   = e^(lse_run - lse') O_run + e^(lse_c - lse') O_c.
+        // A running LSE of -inf is an empty row: weight 0, its O_run is never read.
+        const float run2 = (t ? lse_run1 : lse_run0) * 1.4426950408889634f;
+        const float mx2 = fmaxf(run2, lse2);
+        const float a = ptx::ex2_approx(run2 - mx2);
+        const float b = ptx::ex2_approx(lse2 - mx2);
+        const float sum = a + b;
+        w_run = a / sum;
+        inv_l = (b / sum) * inv_lp;
+        const int row = item.q_row0 + t * kBlockM + r;
+        if (row < p.n_q) p.lse[head_row0 + row] = (mx2 + log2f(sum)) * 0.69314718055994530942f;
+      }
+      const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
+      const int row = row0w + lane;
+      // Accumulate mode: 16 columns of this thread's own row of the running output are
+      // in flight ahead of their use; rows of weight 0 (empty) or past n_q are not read.
+      const bool use_run = kAccum && row < p.n_q && w_run != 0.f;
+      const float* const run_row = p.out_f32 + (head_row0 + row) * D;
+      uint32_t o[16];
+      auto load_run = [&](int k) {
+        if constexpr (kAccum) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            ptx::U32x8 u{};
+            if (use_run) u = ptx::ld_global_32B(run_row + k * 16 + q * 8, p.out_align32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[q * 8 + i] = u.v[i];
+          }
+        }
+      };
+      load_run(0);  // in flight while the last PV finishes
       if (!(ok = wait(L::bPVDone + t, g_last & 1))) break;
       ptx::tc_fence_after();
       if (r == 0 && t == 0) DIT_TRACE(kTrCta, 2 + 2 * li);
       const uint32_t tO = tmem + 2 * kBlockN + t * D + lane_off;
-      const int row = item.q_row0 + t * kBlockM + r;
-      const bool store = row < p.n_q;
-      const size_t out_row = (static_cast<size_t>(item.bh) * p.n_q + row) * D;
-      // Two 32-column chunks per TMEM read; O_t is released as soon as the last chunk is
-      // in registers, before its stores.  Rows are written with 32-byte stores (full
-      // sectors) when the output is 32-byte aligned, else 16-byte stores.  Each warp store
-      // touches 32 rows (32 sectors); a burst of them can hold up the softmax's shared-
-      // memory P writes at the start of the next item, so the stores issued after O_t is
-      // released can be paced kStorePaceNs apart (off by default: on the Wan2.2 workload
-      // pacing trades ~1 % of the fused pass for ~1 % of the chunk path).
-#pragma unroll
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t u[64];
-        {
-          uint32_t a[32], b[32];
-          ptx::tmem_ld32(tO + half * 64, a);
-          ptx::tmem_ld32(tO + half * 64 + 32, b);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            u[i] = a[i];
-            u[32 + i] = b[i];
-          }
-        }
-        if (half == D / 64 - 1) {
-          // O_t has been read: the PV issuer may start the next item's O_t.
+      auto release_if = [&](bool last) {
+        if (last) {  // O_t has been read: the PV issuer may start the next item's O_t.
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar(L::bOEmpty + t));
         }
-        if (!store) continue;
-        auto v = [&](int i) { return __uint_as_float(u[i]) * inv_l; };
-        auto pace = [&]() {
-          if (kStorePaceNs > 0 && half == D / 64 - 1) __nanosleep(kStorePaceNs);
-        };
-        if constexpr (kOutF32) {
-          float* dst = p.out_f32 + out_row + half * 64;
-          if (p.out_align32) {
+      };
+      if constexpr (kOutF32 && !kAccum) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 8) {
-              pace();
-              asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + i),
-                           "f"(v(i)), "f"(v(i + 1)), "f"(v(i + 2)), "f"(v(i + 3)), "f"(v(i + 4)),
-                           "f"(v(i + 5)), "f"(v(i + 6)), "f"(v(i + 7))
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          ptx::tmem_ld32(tO + c * 32, x);
+          ptx::tmem_wait_ld();
+          release_if(c == D / 32 - 1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * inv_l);
+          swap_lane_reg_bit<4, 4>(x, lane);
+          swap_lane_reg_bit<3, 3>(x, lane);
+          // x[8*rr + i] = (row row0w + 8*rr + r_lo, column 32*c + 8*cgrp + i)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int row_k = row0w + rr * 8 + r_lo;
+            if (row_k < p.n_q)
+              st_global_32B(p.out_f32 + (head_row0 + row_k) * D + c * 32 + cgrp * 8, p.out_align32,
+                            &x[rr * 8]);
+          }
+        }
+      } else if constexpr (kAccum) {
+        // 16-column steps: O' = (1/lp)(w_c) O_acc + w_run O_run on the own row, then the
+        // transpose (lane bits 4,3 <-> register bits 3,2) and 8-row x 64-byte stores.
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          uint32_t x[16];
+          ptx::tmem_ld16(tO + k * 16, x);
+          ptx::tmem_wait_ld();
+          release_if(k == D / 16 - 1);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float y = __uint_as_float(x[i]) * inv_l;
+            x[i] = __float_as_uint(use_run ? fmaf(w_run, __uint_as_float(o[i]), y) : y);
+          }
+          if (k + 1 < D / 16) load_run(k + 1);
+          swap_lane_reg_bit<4, 3>(x, lane);
+          swap_lane_reg_bit<3, 2>(x, lane);
+          // x[4*rr + i] = (row row0w + 8*rr + r_lo, column 16*k + 4*cgrp + i)
+#pragma unroll
+          for (int rr = 0; rr < 4; ++rr) {
+            const int row_k = row0w + rr * 8 + r_lo;
+            if (row_k < p.n_q) {
+              float* dst = p.out_f32 + (head_row0 + row_k) * D + k * 16 + cgrp * 4;
+              asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(x[rr * 4]),
+                           "r"(x[rr * 4 + 1]), "r"(x[rr * 4 + 2]), "r"(x[rr * 4 + 3])
                            : "memory");
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-              if (i % 8 == 0) pace();
-              *reinterpret_cast<float4*>(dst + i) = make_float4(v(i), v(i + 1), v(i + 2), v(i + 3));
             }
           }
-        } else {
-          __nv_bfloat16* dst = p.out_bf16 + out_row + half * 64;
-          auto w = [&](int i) { return ptx::pack_bf16x2(v(2 * i), v(2 * i + 1)); };
-          if (p.out_align32) {
+        }
+      } else {
+        __nv_bfloat16* dst = p.out_bf16 + (head_row0 + row) * D;
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              pace();
-              asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 2 * i),
-                           "r"(w(i)), "r"(w(i + 1)), "r"(w(i + 2)), "r"(w(i + 3)), "r"(w(i + 4)),
-                           "r"(w(i + 5)), "r"(w(i + 6)), "r"(w(i + 7))
-                           : "memory");
-            }
-          } else {
+        for (int half = 0; half < D / 64; ++half) {
+          uint32_t wd[32];  // 64 columns of this thread's row as bf16 pairs
+          {
+            uint32_t a[32], b[32];
+            ptx::tmem_ld32(tO + half * 64, a);
+            ptx::tmem_ld32(tO + half * 64 + 32, b);
+            ptx::tmem_wait_ld();
+            release_if(half == D / 64 - 1);
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              if (i % 8 == 0) pace();
-              *reinterpret_cast<uint4*>(dst + 2 * i) = make_uint4(w(i), w(i + 1), w(i + 2), w(i + 3));
+            for (int i = 0; i < 16; ++i) {
+              wd[i] = ptx::pack_bf16x2(__uint_as_float(a[2 * i]) * inv_l,
+                                       __uint_as_float(a[2 * i + 1]) * inv_l);
+              wd[16 + i] = ptx::pack_bf16x2(__uint_as_float(b[2 * i]) * inv_l,
+                                            __uint_as_float(b[2 * i + 1]) * inv_l);
             }
+          }
+          if (row < p.n_q) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
+              st_global_32B(dst + half * 64 + 2 * i, p.out_align32, &wd[i]);
           }
         }
       }
@@ -722,7 +842,7 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
 
 }  // namespace detail
 
-template <int D, bool kOutF32>
+template <int D, bool kOutF32, bool kAccum>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   using L = AttnSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -773,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp < kLoadWarp) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    detail::softmax_wg<D>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles, abort_flag);
+    detail::softmax_wg<D, kAccum>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles, abort_flag);
   } else if (warp < kEpiWarp0) {
     ptx::setmaxnreg_dec<kRegsIssue>();
     if (warp == kLoadWarp) {
@@ -785,8 +905,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     __syncwarp();
   } else {
-    ptx::setmaxnreg_dec<kRegsEpilogue>();
-    detail::epilogue_wg<D, kOutF32>(p, sbase, tmem, warp, lane, n_tiles, abort_flag);
+    ptx::setmaxnreg_dec<kAccum ? kRegsEpilogueAccum : kRegsEpilogue>();
+    detail::epilogue_wg<D, kOutF32, kAccum>(p, sbase, tmem, warp, lane, n_tiles, abort_flag);
   }
 
   ptx::tc_fence_before();

@@ -85,7 +85,8 @@ dit_status validate_attention(const void* q, const void* k, const void* v, const
 
 dit_status run_attention(const void* q, const void* k, const void* v, void* out, float* lse,
                          int B, int H, int N_q, int n_kv, int D, long long kv_head_stride,
-                         float scale, dit_dtype out_dtype, dit_stream stream) {
+                         float scale, dit_dtype out_dtype, dit_stream stream,
+                         bool accumulate = false) {
   int* status = status_ptr();
   if (!status) return DIT_ERR_CUDA;
   ditattn::AttnLaunch a;
@@ -103,6 +104,7 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   a.kv_head_stride = kv_head_stride;
   a.scale = scale;
   a.out_f32 = out_dtype == DIT_F32;
+  a.accumulate = accumulate;
   return ditattn::launch_attention(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DIT_OK
              : DIT_ERR_CUDA;
@@ -129,6 +131,16 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
   if (s != DIT_OK) return s;
   return run_attention(q, k, v, out_partial, lse_partial, B, H, N_q, n_kv, D, kv_head_stride,
                        scale, partial_dtype, stream);
+}
+
+dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const void* v, float* o_run,
+                                         float* lse_run, int B, int H, int N_q, int n_kv, int D,
+                                         long long kv_head_stride, float scale, dit_stream stream) {
+  dit_status s = validate_attention(q, k, v, o_run, lse_run, B, H, N_q, n_kv, D, kv_head_stride,
+                                    scale, DIT_F32);
+  if (s != DIT_OK) return s;
+  return run_attention(q, k, v, o_run, lse_run, B, H, N_q, n_kv, D, kv_head_stride, scale, DIT_F32,
+                       stream, /*accumulate=*/true);
 }
 
 dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,

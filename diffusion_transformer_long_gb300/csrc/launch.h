@@ -21,6 +21,9 @@ struct AttnLaunch {
   long long kv_head_stride;  // elements
   float scale;
   bool out_f32;
+  // Ring-hop accumulate: out (fp32) and lse hold a running (O, lse) that this pass
+  // merges into in place.
+  bool accumulate = false;
 };
 
 // Encodes the TMA descriptors and launches the attention kernel on `st`.

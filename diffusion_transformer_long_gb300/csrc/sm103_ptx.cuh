@@ -270,6 +270,45 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef DITATTN_R8
 #undef DITATTN_W8
 
+// ---------------------------------------------------------------- global memory
+// Volatile so that the load is issued where it is written (early), not next to its use.
+__device__ __forceinline__ float ld_global_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// 32 bytes from global memory: one 32-byte load when src is 32-byte aligned, else two
+// 16-byte ones.
+struct U32x8 {
+  uint32_t v[8];
+};
+__device__ __forceinline__ U32x8 ld_global_32B(const void* src, bool align32) {
+  U32x8 r;
+  if (align32) {
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3]), "=r"(r.v[4]),
+                   "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(src)
+                 : "memory");
+  } else {
+    asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.v[0]), "=r"(r.v[1]), "=r"(r.v[2]), "=r"(r.v[3])
+                 : "l"(src)
+                 : "memory");
+    asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.v[4]), "=r"(r.v[5]), "=r"(r.v[6]), "=r"(r.v[7])
+                 : "l"(static_cast<const char*>(src) + 16)
+                 : "memory");
+  }
+  return r;
+}
+
+// Hint: bring one 128-byte line into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

@@ -19,9 +19,9 @@ from . import build as _build
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
 DIT_F32, DIT_BF16 = 0, 1
 
-EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_chunk_fwd", "dit_attn_lse_merge", "dit_attn_check",
-                    "dit_test_inject_stall", "dit_test_set_grid_limit", "dit_status_string",
-                    "dit_version")
+EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_chunk_fwd", "dit_attn_chunk_fwd_accumulate",
+                    "dit_attn_lse_merge", "dit_attn_check", "dit_test_inject_stall",
+                    "dit_test_set_grid_limit", "dit_status_string", "dit_version")
 
 _lib = None
 
@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
         L.dit_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
         L.dit_attn_chunk_fwd.restype = I
         L.dit_attn_chunk_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, P]
+        L.dit_attn_chunk_fwd_accumulate.restype = I
+        L.dit_attn_chunk_fwd_accumulate.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, P]
         L.dit_attn_lse_merge.restype = I
         L.dit_attn_lse_merge.argtypes = [P, P, I, P, P, I, I, I, I, I, I, P]
         L.dit_attn_check.restype = I
@@ -164,6 +166,34 @@ def attn_chunk_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.floa
     return out, lse
 
 
+def attn_chunk_fwd_accumulate(q, k, v, o_run, lse_run, scale=None, stream=None):
+    """One ring hop with the merge fused in: the attention of q against one KV chunk (a view such
+    as k[:, :, s:s+n] or a packed buffer) merged in place into the running o_run (fp32
+    [B, H, N_q, D]) and lse_run (fp32 [B, H, N_q]).  Rows with lse_run = -inf are empty: their
+    o_run is not read.  Returns (o_run, lse_run)."""
+    _check_qkv(q, k, v)
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v chunk must be [B, H, n_kv, D] matching q")
+    hs = kv_head_stride(k)
+    if kv_head_stride(v) != hs:
+        raise ValueError("k and v chunks must have the same head stride")
+    if (o_run.dtype != torch.float32 or tuple(o_run.shape) != (B, H, Nq, D)
+            or not o_run.is_contiguous() or o_run.device != q.device):
+        raise ValueError("o_run must be a contiguous fp32 [B, H, N_q, D] tensor on q's device")
+    if (lse_run.dtype != torch.float32 or tuple(lse_run.shape) != (B, H, Nq)
+            or not lse_run.is_contiguous() or lse_run.device != q.device):
+        raise ValueError("lse_run must be a contiguous fp32 [B, H, N_q] tensor on q's device")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_chunk_fwd_accumulate(_ptr(q), _ptr(k), _ptr(v), _ptr(o_run),
+                                                 _ptr(lse_run), B, H, Nq, k.shape[2], D, hs, scale,
+                                                 _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_chunk_fwd_accumulate")
+    return o_run, lse_run
+
+
 def attn_lse_merge(partials, lses, out=None, lse=None, out_dtype=torch.float32, stream=None):
     """Merge p partials [p, B, H, N, D] (fp32 or bf16) with lses fp32 [p, B, H, N]."""
     if not partials.is_cuda or partials.dim() != 5 or not partials.is_contiguous():
@@ -224,11 +254,33 @@ def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,
     return attn_lse_merge(partials, lses, out_dtype=out_dtype, stream=stream)
 
 
+def ring_attention(q, k, v, chunks, scale=None, o_run=None, lse_run=None, stream=None):
+    """Ring decomposition on one GPU with the merge fused into each hop: the running (o_run,
+    lse_run) starts empty (lse_run = -inf) and every KV chunk (virtual rank) is folded in by one
+    dit_attn_chunk_fwd_accumulate.  `chunks` lists the chunk lengths (sum = N_kv).  Returns
+    (o_run fp32, lse_run)."""
+    B, H, Nq, D = q.shape
+    if sum(chunks) != k.shape[2] or any(n < 1 for n in chunks):
+        raise ValueError("chunk lengths must be positive and sum to the number of keys")
+    if o_run is None:
+        o_run = torch.empty((B, H, Nq, D), device=q.device, dtype=torch.float32)
+    if lse_run is None:
+        lse_run = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    lse_run.fill_(float("-inf"))
+    s = 0
+    for n in chunks:
+        attn_chunk_fwd_accumulate(q, k[:, :, s:s + n], v[:, :, s:s + n], o_run, lse_run,
+                                  scale=scale, stream=stream)
+        s += n
+    return o_run, lse_run
+
+
 def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
-              partial_dtype=torch.float32, device=None):
+              partial_dtype=torch.float32, device=None, accumulate=False):
     """User-level call.  Accepts CUDA tensors, or CPU tensors (ideally pinned) that are copied to
     the device and whose results are copied back.  chunks=None runs the fused pass; a list of
-    chunk lengths runs the p-chunk ring decomposition with the LSE merge."""
+    chunk lengths runs the p-chunk ring decomposition, merged by a separate LSE-merge pass or,
+    with accumulate=True, hop by hop inside each chunk pass (fp32 output)."""
     on_host = not q.is_cuda
     if on_host:
         dev = torch.device("cuda") if device is None else torch.device(device)
@@ -237,6 +289,10 @@ def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
         v = v.to(dev, non_blocking=True)
     if chunks is None:
         out, lse = attn_fwd(q, k, v, scale=scale, out_dtype=out_dtype)
+    elif accumulate:
+        if out_dtype != torch.float32:
+            raise ValueError("the hop-by-hop ring accumulates in fp32")
+        out, lse = ring_attention(q, k, v, chunks, scale=scale)
     else:
         out, lse = chunk_attention(q, k, v, chunks, scale=scale, out_dtype=out_dtype,
                                    partial_dtype=partial_dtype)

@@ -4,8 +4,10 @@
  * The library computes O = softmax(scale * Q K^T) V per (batch, head) over
  * long token sequences, either in one fused pass or as p KV chunks whose
  * partial outputs and log-sum-exps are merged exactly as one Ring-attention
- * hop merges them.  On one GPU the p chunks are virtual ranks: a "hop" is a
- * pointer to the next chunk, with no communication.
+ * hop merges them: by a separate merge of the p stacked partials, or hop by
+ * hop into a running output inside each chunk pass.  On one GPU the p chunks
+ * are virtual ranks: a "hop" is a pointer to the next chunk, with no
+ * communication.
  *
  * Conventions shared by every entry point:
  *  - Tensors are plain device pointers, contiguous row-major [B, H, N, D]
@@ -86,6 +88,30 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
                               float* lse_partial, int B, int H, int N_q, int n_kv, int D,
                               long long kv_head_stride, float scale, dit_dtype partial_dtype,
                               dit_stream stream);
+
+/*
+ * One Ring-attention hop with the merge fused into the chunk pass: the attention
+ * of all N_q queries against ONE KV chunk, (O_c, lse_c) exactly as
+ * dit_attn_chunk_fwd defines them, is merged in place into a running output:
+ *   M = max(lse_run, lse_c);  lse' = M + ln(exp(lse_run - M) + exp(lse_c - M));
+ *   O' = exp(lse_run - lse') O_run + exp(lse_c - lse') O_c
+ * which is the online-softmax accumulation a Ring round performs on the block it
+ * receives (arganzheng.life, section 4.2 Ring).  Applying it once per chunk of
+ * the keys, in any order, gives the full attention.  No stacked partials and no
+ * separate merge pass.
+ *   q, k, v, B, H, N_q, n_kv, D, kv_head_stride, scale : as dit_attn_chunk_fwd
+ *   o_run   : device fp32 [B, H, N_q, D], 16-byte aligned (read and written)
+ *   lse_run : device fp32 [B, H, N_q], 4-byte aligned (read and written)
+ * A row whose lse_run is -inf is empty: its o_run is never read (it may hold
+ * anything, NaN included) and the row becomes this chunk's own attention.  So a
+ * running state starts either as lse_run = -inf everywhere (o_run
+ * uninitialised) or as the fp32 output of dit_attn_chunk_fwd for the first
+ * chunk.  o_run and lse_run must not overlap each other or q, k, v
+ * (DIT_ERR_INVALID_ARG).  Rows whose lse_run is +inf or NaN propagate NaN.
+ */
+dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const void* v, float* o_run,
+                                         float* lse_run, int B, int H, int N_q, int n_kv, int D,
+                                         long long kv_head_stride, float scale, dit_stream stream);
 
 /*
  * Exact merge of p chunk partials (O_c, lse_c) of the same queries:

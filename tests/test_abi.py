@@ -97,6 +97,39 @@ def test_chunk_validation(lib, kw, status):
     assert chunk(lib, **kw) == status
 
 
+def accumulate(lib, n_kv=100, hs=256 * 128, D=128, **kw):
+    args = dict(q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, scale=0.088)
+    args.update(kw)
+    return lib.dit_attn_chunk_fwd_accumulate(args["q"], args["k"], args["v"], args["out"],
+                                             args["lse"], args["B"], args["H"], args["N"], n_kv, D,
+                                             hs, args["scale"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_kv=0), da.DIT_ERR_INVALID_ARG), (dict(N=0), da.DIT_ERR_INVALID_ARG),
+    (dict(n_kv=300, hs=256 * 128), da.DIT_ERR_INVALID_ARG),   # stride shorter than the chunk
+    (dict(hs=256 * 128 + 4), da.DIT_ERR_INVALID_ARG),
+    (dict(D=96), da.DIT_ERR_UNSUPPORTED),
+    (dict(out=None), da.DIT_ERR_INVALID_ARG), (dict(lse=None), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((4 << 40) + 8)), da.DIT_ERR_INVALID_ARG),     # o_run not 16-aligned
+    (dict(lse=ctypes.c_void_p((5 << 40) + 2)), da.DIT_ERR_INVALID_ARG),
+    (dict(scale=math.nan), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((3 << 40) + 64)), da.DIT_ERR_INVALID_ARG),     # o_run inside v
+    (dict(lse=ctypes.c_void_p((4 << 40) + 1024)), da.DIT_ERR_INVALID_ARG),  # lse_run inside o_run
+])
+def test_accumulate_validation(lib, kw, status):
+    assert accumulate(lib, **kw) == status
+
+
+def test_accumulate_binding_checks_running_state(lib):
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    o = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):           # host tensors
+        da.attn_chunk_fwd_accumulate(x, x, x, o, torch.zeros(1, 1, 8))
+    with pytest.raises(ValueError):           # chunk lengths must cover the keys
+        da.ring_attention(x, x, x, [3, 4])
+
+
 def merge(lib, p=4, parts=Q, lses=K, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, pdt=0, odt=0):
     return lib.dit_attn_lse_merge(parts, lses, p, out, lse, B, H, N, D, pdt, odt, None)
 

@@ -109,6 +109,22 @@ def test_chunk_merge_bf16_partials(workload):
     assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} bf16 partials", bf16_out=True)
 
 
+def test_ring_accumulate(workload):
+    """Hop-by-hop ring: every chunk folded into the running (O, lse) by
+    dit_attn_chunk_fwd_accumulate.  The running output starts as NaN with lse = -inf, which
+    also checks that empty rows' O_run is never read."""
+    w, q, k, v, rows, o_ref, lse_ref = workload
+    B, H, N, D = q.shape
+    for chunks, what in ((w.chunks, f"p={w.p}"), (w.alt_chunks, "uneven")):
+        if not chunks:
+            continue
+        o_run = torch.full((B, H, N, D), math.nan, device=DEV)
+        o, lse = da.ring_attention(q, k, v, chunks, scale=w.scale, o_run=o_run)
+        da.check()
+        assert o.data_ptr() == o_run.data_ptr()
+        assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"{w.name} ring accumulate {what}")
+
+
 def test_chunk_partials_match_oracle_chunks(workload):
     """Each virtual rank's partial (O_c, lse_c) against the oracle over that chunk alone."""
     w, q, k, v, rows, _, _ = workload
@@ -352,10 +368,12 @@ def test_persistent_grid_many_items_per_cta(limit):
             o, lse = da.attn_fwd(qd, kd, vd, scale=scale)
             ob, lb = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=torch.bfloat16)
             oc, lc = da.chunk_attention(qd, kd, vd, (1, 127, 128, 129, 315), scale=scale)
+            orr, lrr = da.ring_attention(qd, kd, vd, (1, 127, 128, 129, 315), scale=scale)
             da.check()
             assert_parity(o, lse, o_ref, lse_ref, f"grid={limit} D={D} fused")
             assert_parity(ob, lb, o_ref, lse_ref, f"grid={limit} D={D} bf16", bf16_out=True)
             assert_parity(oc, lc, o_ref, lse_ref, f"grid={limit} D={D} chunks")
+            assert_parity(orr, lrr, o_ref, lse_ref, f"grid={limit} D={D} ring accumulate")
     finally:
         da.set_grid_limit(0)
 
