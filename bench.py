@@ -379,6 +379,62 @@ def run_gpu(args):
     ring_ms = max_over_ranks(dist, r0.elapsed_time(r1) / nr)
     ring_diff = (out_f - out_c).abs().max().item()
 
+    # ---- token-major (BSND) tensors: the re-shard transpose and attention on strided views ----
+    q_s = da.bhnd_to_bsnd(q)                       # [B, N, H, D] memory
+    k_s, v_s = da.bhnd_to_bsnd(k), da.bhnd_to_bsnd(v)
+    out_s = torch.empty((B, N, H, D), device=dev, dtype=torch.float32)
+    q_t = torch.empty_like(q)
+    for _ in range(args.warmup):
+        da.bsnd_to_bhnd(q_s, out=q_t)
+        da.attn_fwd_strided(q_s.transpose(1, 2), k_s.transpose(1, 2), v_s.transpose(1, 2),
+                            out=out_s.transpose(1, 2), lse=lse_c, scale=w.scale)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    bsnd_diff = (out_s.transpose(1, 2) - out_f).abs().max().item()
+    t_0, t_1 = ev(), ev()
+    nt = max(10, args.steps)
+    t_0.record(stream)
+    for _ in range(nt):
+        da.bsnd_to_bhnd(q_s, out=q_t)
+    t_1.record(stream)
+    a_0, a_1 = ev(), ev()
+    na = max(3, args.steps // 3)
+    a_0.record(stream)
+    for _ in range(na):
+        da.attn_fwd_strided(q_s.transpose(1, 2), k_s.transpose(1, 2), v_s.transpose(1, 2),
+                            out=out_s.transpose(1, 2), lse=lse_c, scale=w.scale)
+    a_1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    transpose_ms = max_over_ranks(dist, t_0.elapsed_time(t_1) / nt)
+    transpose_bytes = 2 * B * H * N * D * 2
+    bsnd_ms = max_over_ranks(dist, a_0.elapsed_time(a_1) / na)
+    del q_s, k_s, v_s, out_s, q_t
+
+    # ---- stale-KV attention of one patch (displaced patch parallelism, p patches) ----
+    m = w.chunks[0]
+    kb, vb = k.clone(), v.clone()
+    q_patch = q[:, :, :m].contiguous()
+    k_new, v_new = k[:, :, :m].contiguous(), v[:, :, :m].contiguous()
+    o_patch = torch.empty((B, H, m, D), device=dev, dtype=torch.float32)
+    l_patch = torch.empty((B, H, m), device=dev, dtype=torch.float32)
+    for _ in range(args.warmup):
+        da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
+                              scale=w.scale)
+    torch.cuda.synchronize(dev)
+    st_0, st_1 = ev(), ev()
+    ns = max(5, args.steps)
+    st_0.record(stream)
+    for _ in range(ns):
+        da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
+                              scale=w.scale)
+    st_1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    stale_ms = max_over_ranks(dist, st_0.elapsed_time(st_1) / ns)
+    stale_flops = 4.0 * B * H * m * N * D
+    del kb, vb, q_patch, k_new, v_new, o_patch, l_patch
+
     # ---- cross-attention shape: all N queries against 512 replicated text keys ----
     n_txt = 512
     kx, vx = k[:, :, :n_txt], v[:, :, :n_txt]
@@ -473,6 +529,14 @@ def run_gpu(args):
                                     "tflops": w.flops / (ring_ms * 1e-3) / 1e12,
                                     "ratio_to_fused": ring_ms / fused_ms,
                                     "max_abs_vs_fused": ring_diff},
+                "fused_bsnd_layout": {"ms": bsnd_ms, "tflops": w.flops / (bsnd_ms * 1e-3) / 1e12,
+                                      "max_abs_vs_bhnd": bsnd_diff},
+                "bsnd_to_bhnd_transpose": {"ms": transpose_ms,
+                                           "gbs": transpose_bytes / (transpose_ms * 1e-3) / 1e9,
+                                           "frac_of_hbm": transpose_bytes / (transpose_ms * 1e-3)
+                                           / 1e9 / hbm},
+                "stale_kv_patch": {"ms": stale_ms, "queries": m, "keys": N,
+                                   "tflops": stale_flops / (stale_ms * 1e-3) / 1e12},
                 "cross_attention_512_text_keys": {"ms": cross_ms,
                                                   "tflops": cross_flops / (cross_ms * 1e-3) / 1e12},
                 "fused_vs_chunk_max_abs": diff,

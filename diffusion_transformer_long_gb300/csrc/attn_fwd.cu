@@ -50,19 +50,20 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-// 3-D bf16 map (d, rows, heads) with 128-row x 64-column boxes and 128-byte
-// swizzle; rows past `rows` read as zero.
-bool encode_bhnd(CUtensorMap* m, const void* base, int d, int rows, int heads,
-                 long long head_stride_elems) {
+// 4-D bf16 map (d, rows, heads, batch) of a strided [B, H, rows, d] view, with
+// 128-row x 64-column boxes and 128-byte swizzle; rows past `rows` read as zero.
+bool encode_view(CUtensorMap* m, const void* base, int d, int rows, int heads, int batch,
+                 const Strides& st) {
   EncodeTiledFn fn = encoder();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
-                              static_cast<cuuint64_t>(heads)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(head_stride_elems) * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockM), 1};
-  const cuuint32_t elem_strides[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n_) * 2,
+                                 static_cast<cuuint64_t>(st.h_) * 2,
+                                 static_cast<cuuint64_t>(st.b_) * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockM), 1, 1};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -87,20 +88,29 @@ cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
 
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   AttnParams prm;
-  if (!encode_bhnd(&prm.tm_q, a.q, a.d, a.n_q, a.bh, a.q_head_stride) ||
-      !encode_bhnd(&prm.tm_k, a.k, a.d, a.n_kv, a.bh, a.kv_head_stride) ||
-      !encode_bhnd(&prm.tm_v, a.v, a.d, a.n_kv, a.bh, a.kv_head_stride))
+  if (!encode_view(&prm.tm_q, a.q, a.d, a.n_q, a.heads, a.batch, a.qs) ||
+      !encode_view(&prm.tm_k, a.k, a.d, a.n_kv, a.heads, a.batch, a.ks) ||
+      !encode_view(&prm.tm_v, a.v, a.d, a.n_kv, a.heads, a.batch, a.vs))
     return cudaErrorInvalidValue;
   prm.out_f32 = a.out_f32 ? static_cast<float*>(a.out) : nullptr;
   prm.out_bf16 = a.out_f32 ? nullptr : static_cast<__nv_bfloat16*>(a.out);
-  prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) % 32) == 0 ? 1 : 0;
+  prm.o_sb = a.os.b_;
+  prm.o_sh = a.os.h_;
+  prm.o_sn = a.os.n_;
+  // 32-byte row segments need the base and every stride (in bytes) 32-byte aligned.
+  const long long esize = a.out_f32 ? 4 : 2;
+  prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0 && (a.os.b_ * esize) % 32 == 0 &&
+                     (a.os.h_ * esize) % 32 == 0 && (a.os.n_ * esize) % 32 == 0)
+                        ? 1
+                        : 0;
   prm.lse = a.lse;
   prm.status = a.status;
   prm.n_q = a.n_q;
   prm.n_kv = a.n_kv;
-  prm.bh_count = a.bh;
+  prm.bh_count = a.batch * a.heads;
+  prm.heads = a.heads;
   prm.q_pairs = (a.n_q + 2 * kBlockM - 1) / (2 * kBlockM);
-  prm.num_items = prm.q_pairs * a.bh;
+  prm.num_items = prm.q_pairs * prm.bh_count;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;
   prm.stall_kv = g_stall_kv;

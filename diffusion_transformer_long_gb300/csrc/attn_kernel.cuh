@@ -107,14 +107,16 @@ struct AttnParams {
   CUtensorMap tm_q;   // (D, n_q, bh) bf16, box (64, 128, 1), 128B swizzle
   CUtensorMap tm_k;   // (D, n_kv, bh), head stride = kv_head_stride
   CUtensorMap tm_v;
-  float* out_f32;     // [bh, n_q, D] (fp32 output) or null
-  __nv_bfloat16* out_bf16;  // [bh, n_q, D] (bf16 output) or null
-  int out_align32;    // the output base is 32-byte aligned (full-sector stores)
-  float* lse;         // [bh, n_q]
+  float* out_f32;     // (fp32 output) or null; O[b][h][n][d] at b*o_sb + h*o_sh + n*o_sn + d
+  __nv_bfloat16* out_bf16;  // (bf16 output) or null; same addressing
+  long long o_sb, o_sh, o_sn;  // output strides in elements
+  int out_align32;    // base and strides keep every row segment 32-byte aligned
+  float* lse;         // [bh, n_q] contiguous
   int* status;        // device status word (timeouts)
   int n_q;
   int n_kv;
   int bh_count;
+  int heads;          // H: head bh is (b, h) = (bh / H, bh % H)
   int q_pairs;        // ceil(n_q / 256)
   int num_items;      // bh_count * q_pairs
   float scale_log2;   // scale * log2(e)
@@ -178,11 +180,17 @@ __device__ __forceinline__ void raise_abort(const AttnParams& p, volatile int* a
 }
 
 struct Item {
-  int bh;
-  int q_row0;
+  int bh;      // b * H + h
+  int b, h;
+  int q_row0;  // first query row of the pair of Q tiles
+  __device__ __forceinline__ size_t out_off(const AttnParams& p) const {
+    return static_cast<size_t>(b) * p.o_sb + static_cast<size_t>(h) * p.o_sh;
+  }
 };
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
-  return {w / p.q_pairs, (w % p.q_pairs) * 2 * kBlockM};
+  const int bh = w / p.q_pairs;
+  const int b = bh / p.heads;
+  return {bh, b, bh - b * p.heads, (w % p.q_pairs) * 2 * kBlockM};
 }
 
 // K/V ring items of one work item, in consumption order: K_0, then per KV tile j:
@@ -216,7 +224,7 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
   int q_loads = 0;  // Q loads issued (QFULL phases armed)
   int it = 0;       // ring index
   bool ok = true;
-  auto load = [&](bool is_v, int tile, int bh) {
+  auto load = [&](bool is_v, int tile, const Item& item) {
     const int s = it % kStages;
     const uint32_t ph = (it / kStages) & 1;
     if (!wait(L::bKVEmpty + s, ph ^ 1)) return false;
@@ -228,8 +236,8 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     const CUtensorMap* tm = is_v ? &p.tm_v : &p.tm_k;
 #pragma unroll
     for (int r = 0; r < kRegions; ++r)
-      ptx::tma_load_3d(sbase + L::kKV + s * L::kTile + r * L::kRegion, tm, bar(fb), r * 64,
-                       tile * kBlockN, bh);
+      ptx::tma_load_4d(sbase + L::kKV + s * L::kTile + r * L::kRegion, tm, bar(fb), r * 64,
+                       tile * kBlockN, item.h, item.b);
     DIT_TRACE(kTrProdIssue, it);
 #pragma unroll
     for (int q = 0; q < kStages; ++q)
@@ -250,16 +258,16 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     for (int t = 0; t < 2; ++t)
 #pragma unroll
       for (int r = 0; r < kRegions; ++r)
-        ptx::tma_load_3d(sbase + (t ? L::kQ1 : L::kQ0) + r * L::kRegion, &p.tm_q,
-                         bar(L::bQFull), r * 64, item.q_row0 + t * kBlockM, item.bh);
+        ptx::tma_load_4d(sbase + (t ? L::kQ1 : L::kQ0) + r * L::kRegion, &p.tm_q,
+                         bar(L::bQFull), r * 64, item.q_row0 + t * kBlockM, item.h, item.b);
     DIT_TRACE(kTrQIssue, q_loads);
     ++q_loads;
     if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
 
-    if (!(ok = load(false, 0, item.bh))) break;
+    if (!(ok = load(false, 0, item))) break;
     for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j + 1 < n_tiles && !(ok = load(false, j + 1, item.bh))) break;
-      ok = load(true, j, item.bh);
+      if (j + 1 < n_tiles && !(ok = load(false, j + 1, item))) break;
+      ok = load(true, j, item);
     }
   }
   if (!ok) {
@@ -690,7 +698,8 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
     const Item item = item_of(p, w);
     const int g_last = (li + 1) * n_tiles - 1;  // CTA-global index of the item's last tile
-    const size_t head_row0 = static_cast<size_t>(item.bh) * p.n_q;
+    const size_t head_row0 = static_cast<size_t>(item.bh) * p.n_q;  // LSE rows
+    const size_t out_off = item.out_off(p);                           // output head
     // Accumulate mode: this item's running LSEs (read now, long before they are needed)
     // and its running-output rows brought into L2 while the item runs.
     float lse_run0 = -INFINITY, lse_run1 = -INFINITY;
@@ -701,7 +710,7 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
         if (row < p.n_q) {
           (t ? lse_run1 : lse_run0) = ptx::ld_global_f32(p.lse + head_row0 + row);
 #pragma unroll
-          for (int q = 0; q < D / 32; ++q) ptx::prefetch_l2(p.out_f32 + (head_row0 + row) * D + q * 32);
+          for (int q = 0; q < D / 32; ++q) ptx::prefetch_l2(p.out_f32 + out_off + row * p.o_sn + q * 32);
         }
       }
     }
@@ -732,10 +741,11 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
       }
       const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
       const int row = row0w + lane;
-      // Accumulate mode: 16 columns of this thread's own row of the running output are
-      // in flight ahead of their use; rows of weight 0 (empty) or past n_q are not read.
+      // Accumulate mode: the next 16-column piece of this thread's own row of the running
+      // output is in flight while the current one is processed; rows of weight 0 (empty)
+      // or past n_q are not read (their o stays 0).
       const bool use_run = kAccum && row < p.n_q && w_run != 0.f;
-      const float* const run_row = p.out_f32 + (head_row0 + row) * D;
+      const float* const run_row = p.out_f32 + out_off + row * p.o_sn;
       uint32_t o[16];
       auto load_run = [&](int k) {
         if constexpr (kAccum) {
@@ -775,7 +785,7 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
           for (int rr = 0; rr < 4; ++rr) {
             const int row_k = row0w + rr * 8 + r_lo;
             if (row_k < p.n_q)
-              st_global_32B(p.out_f32 + (head_row0 + row_k) * D + c * 32 + cgrp * 8, p.out_align32,
+              st_global_32B(p.out_f32 + out_off + row_k * p.o_sn + c * 32 + cgrp * 8, p.out_align32,
                             &x[rr * 8]);
           }
         }
@@ -789,10 +799,8 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
           ptx::tmem_wait_ld();
           release_if(k == D / 16 - 1);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float y = __uint_as_float(x[i]) * inv_l;
-            x[i] = __float_as_uint(use_run ? fmaf(w_run, __uint_as_float(o[i]), y) : y);
-          }
+          for (int i = 0; i < 16; ++i)
+            x[i] = __float_as_uint(fmaf(w_run, __uint_as_float(o[i]), __uint_as_float(x[i]) * inv_l));
           if (k + 1 < D / 16) load_run(k + 1);
           swap_lane_reg_bit<4, 3>(x, lane);
           swap_lane_reg_bit<3, 2>(x, lane);
@@ -801,7 +809,7 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
           for (int rr = 0; rr < 4; ++rr) {
             const int row_k = row0w + rr * 8 + r_lo;
             if (row_k < p.n_q) {
-              float* dst = p.out_f32 + (head_row0 + row_k) * D + k * 16 + cgrp * 4;
+              float* dst = p.out_f32 + out_off + row_k * p.o_sn + k * 16 + cgrp * 4;
               asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(x[rr * 4]),
                            "r"(x[rr * 4 + 1]), "r"(x[rr * 4 + 2]), "r"(x[rr * 4 + 3])
                            : "memory");
@@ -809,7 +817,7 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
           }
         }
       } else {
-        __nv_bfloat16* dst = p.out_bf16 + (head_row0 + row) * D;
+        __nv_bfloat16* dst = p.out_bf16 + out_off + row * p.o_sn;
 #pragma unroll
         for (int half = 0; half < D / 64; ++half) {
           uint32_t wd[32];  // 64 columns of this thread's row as bf16 pairs

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "../../include/ditattn.h"
 #include "launch.h"
@@ -83,10 +84,44 @@ dit_status validate_attention(const void* q, const void* k, const void* v, const
   return DIT_OK;
 }
 
-dit_status run_attention(const void* q, const void* k, const void* v, void* out, float* lse,
-                         int B, int H, int N_q, int n_kv, int D, long long kv_head_stride,
-                         float scale, dit_dtype out_dtype, dit_stream stream,
-                         bool accumulate = false) {
+// Bytes spanned by a strided [B, H, N, D] view (from its base to one past its last element).
+long long view_span(const dit_strides& s, long long B, long long H, long long N, long long D,
+                    int esize) {
+  return ((B - 1) * s.b + (H - 1) * s.h + (N - 1) * s.n + D) * esize;
+}
+
+dit_strides contiguous(long long H, long long N, long long D) { return {H * N * D, N * D, D}; }
+
+// A strided view usable by the kernels: strides positive multiples of 8 elements (16-byte
+// TMA strides) below 2^39, and the view must fit 64-bit byte offsets comfortably.
+bool valid_strides(const dit_strides& s) {
+  for (long long x : {s.b, s.h, s.n})
+    if (x < 8 || x % 8 != 0 || x >= (1LL << 39)) return false;
+  return true;
+}
+
+// True if no two elements of the view share an address: sorted by stride, every stride
+// must clear the span of the dimensions below it.
+bool no_self_overlap(const dit_strides& s, long long B, long long H, long long N, long long D) {
+  struct Dim {
+    long long stride, extent;
+  } d[3] = {{s.n, N}, {s.h, H}, {s.b, B}};
+  for (int i = 0; i < 3; ++i)  // sort by stride
+    for (int j = i + 1; j < 3; ++j)
+      if (d[j].stride < d[i].stride) std::swap(d[i], d[j]);
+  long long span = D;
+  for (const Dim& x : d) {
+    if (x.extent <= 1) continue;
+    if (x.stride < span) return false;
+    span = x.stride * (x.extent - 1) + span;
+  }
+  return true;
+}
+
+dit_status run_attention(const void* q, const dit_strides& qs, const void* k, const dit_strides& ks,
+                         const void* v, const dit_strides& vs, void* out, const dit_strides& os,
+                         float* lse, int B, int H, int N_q, int n_kv, int D, float scale,
+                         dit_dtype out_dtype, dit_stream stream, bool accumulate = false) {
   int* status = status_ptr();
   if (!status) return DIT_ERR_CUDA;
   ditattn::AttnLaunch a;
@@ -96,18 +131,31 @@ dit_status run_attention(const void* q, const void* k, const void* v, void* out,
   a.out = out;
   a.lse = lse;
   a.status = status;
-  a.bh = B * H;
+  a.batch = B;
+  a.heads = H;
   a.n_q = N_q;
   a.n_kv = n_kv;
   a.d = D;
-  a.q_head_stride = static_cast<long long>(N_q) * D;
-  a.kv_head_stride = kv_head_stride;
+  a.qs = {qs.b, qs.h, qs.n};
+  a.ks = {ks.b, ks.h, ks.n};
+  a.vs = {vs.b, vs.h, vs.n};
+  a.os = {os.b, os.h, os.n};
   a.scale = scale;
   a.out_f32 = out_dtype == DIT_F32;
   a.accumulate = accumulate;
   return ditattn::launch_attention(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DIT_OK
              : DIT_ERR_CUDA;
+}
+
+// Contiguous q/out, K/V heads kv_head_stride elements apart (the chunk form).
+dit_status run_contiguous(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                          int H, int N_q, int n_kv, int D, long long kv_head_stride, float scale,
+                          dit_dtype out_dtype, dit_stream stream, bool accumulate = false) {
+  const dit_strides qs = contiguous(H, N_q, D);
+  const dit_strides kvs = {H * kv_head_stride, kv_head_stride, D};
+  return run_attention(q, qs, k, kvs, v, kvs, out, qs, lse, B, H, N_q, n_kv, D, scale, out_dtype,
+                       stream, accumulate);
 }
 
 }  // namespace
@@ -119,7 +167,7 @@ dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, 
   const long long hs = static_cast<long long>(N) * D;
   dit_status s = validate_attention(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype);
   if (s != DIT_OK) return s;
-  return run_attention(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype, stream);
+  return run_contiguous(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype, stream);
 }
 
 dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out_partial,
@@ -129,8 +177,8 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
   dit_status s = validate_attention(q, k, v, out_partial, lse_partial, B, H, N_q, n_kv, D,
                                     kv_head_stride, scale, partial_dtype);
   if (s != DIT_OK) return s;
-  return run_attention(q, k, v, out_partial, lse_partial, B, H, N_q, n_kv, D, kv_head_stride,
-                       scale, partial_dtype, stream);
+  return run_contiguous(q, k, v, out_partial, lse_partial, B, H, N_q, n_kv, D, kv_head_stride,
+                        scale, partial_dtype, stream);
 }
 
 dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const void* v, float* o_run,
@@ -139,8 +187,133 @@ dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const voi
   dit_status s = validate_attention(q, k, v, o_run, lse_run, B, H, N_q, n_kv, D, kv_head_stride,
                                     scale, DIT_F32);
   if (s != DIT_OK) return s;
-  return run_attention(q, k, v, o_run, lse_run, B, H, N_q, n_kv, D, kv_head_stride, scale, DIT_F32,
-                       stream, /*accumulate=*/true);
+  return run_contiguous(q, k, v, o_run, lse_run, B, H, N_q, n_kv, D, kv_head_stride, scale, DIT_F32,
+                        stream, /*accumulate=*/true);
+}
+
+dit_status dit_attn_fwd_strided(const void* q, const dit_strides* q_strides, const void* k,
+                                const dit_strides* k_strides, const void* v,
+                                const dit_strides* v_strides, void* out,
+                                const dit_strides* out_strides, float* lse, int B, int H, int N_q,
+                                int n_kv, int D, float scale, dit_dtype out_dtype,
+                                dit_stream stream) {
+  dit_status s = check_dims(B, H, N_q, D);
+  if (s != DIT_OK) return s;
+  if (n_kv < 1 || n_kv > INT_MAX) return DIT_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !lse) return DIT_ERR_INVALID_ARG;
+  if (!valid_dtype(out_dtype)) return DIT_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DIT_ERR_INVALID_ARG;
+  // The stride of a size-1 dimension addresses nothing: any valid value will do.
+  auto norm = [&](const dit_strides* p, long long n_rows) {
+    dit_strides x = p ? *p : contiguous(H, n_rows, D);
+    if (B == 1) x.b = D;
+    if (H == 1) x.h = D;
+    if (n_rows == 1) x.n = D;
+    return x;
+  };
+  const dit_strides qs = norm(q_strides, N_q), ks = norm(k_strides, n_kv),
+                    vs = norm(v_strides, n_kv), os = norm(out_strides, N_q);
+  for (const dit_strides* x : {&qs, &ks, &vs, &os})
+    if (!valid_strides(*x)) return DIT_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(lse, 4))
+    return DIT_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (((static_cast<long long>(N_q) + 255) / 256) * bh > INT_MAX) return DIT_ERR_INVALID_ARG;
+  const int oes = dtype_bytes(out_dtype);
+  if (!no_self_overlap(os, B, H, N_q, D)) return DIT_ERR_INVALID_ARG;
+  const Range rq = span(q, view_span(qs, B, H, N_q, D, 2));
+  const Range rk = span(k, view_span(ks, B, H, n_kv, D, 2));
+  const Range rv = span(v, view_span(vs, B, H, n_kv, D, 2));
+  const Range ro = span(out, view_span(os, B, H, N_q, D, oes));
+  const Range rl = span(lse, bh * N_q * 4);
+  for (Range in : {rq, rk, rv})
+    if (overlap(ro, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
+  if (overlap(ro, rl)) return DIT_ERR_INVALID_ARG;
+  return run_attention(q, qs, k, ks, v, vs, out, os, lse, B, H, N_q, n_kv, D, scale, out_dtype,
+                       stream);
+}
+
+dit_status dit_layout_copy(const void* src, const dit_strides* src_strides, void* dst,
+                           const dit_strides* dst_strides, int B, int H, int N, int D,
+                           dit_dtype dtype, dit_stream stream) {
+  dit_status s = check_dims(B, H, N, D);
+  if (s != DIT_OK) return s;
+  if (!src || !dst || !valid_dtype(dtype)) return DIT_ERR_INVALID_ARG;
+  if (!aligned(src, 16) || !aligned(dst, 16)) return DIT_ERR_INVALID_ARG;
+  const int es = dtype_bytes(dtype);
+  auto norm = [&](const dit_strides* p) {
+    dit_strides x = p ? *p : contiguous(H, N, D);
+    if (B == 1) x.b = D;
+    if (H == 1) x.h = D;
+    if (N == 1) x.n = D;
+    return x;
+  };
+  const dit_strides ss = norm(src_strides), ds = norm(dst_strides);
+  if (!valid_strides(ss) || !valid_strides(ds)) return DIT_ERR_INVALID_ARG;
+  if (!no_self_overlap(ds, B, H, N, D)) return DIT_ERR_INVALID_ARG;
+  if (overlap(span(src, view_span(ss, B, H, N, D, es)), span(dst, view_span(ds, B, H, N, D, es))))
+    return DIT_ERR_INVALID_ARG;
+  // One block per (b, h) and run of 256 / (D * es / 16) * 4 rows; the run count is a grid y.
+  const long long rows_per_block = (256 / (D * es / 16)) * 4;
+  if ((N + rows_per_block - 1) / rows_per_block > 65535) return DIT_ERR_UNSUPPORTED;
+  ditattn::CopyLaunch a;
+  a.src = src;
+  a.dst = dst;
+  a.ss = {ss.b, ss.h, ss.n};
+  a.ds = {ds.b, ds.h, ds.n};
+  a.batch = B;
+  a.heads = H;
+  a.n = N;
+  a.d = D;
+  a.elem_bytes = es;
+  return ditattn::launch_layout_copy(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? DIT_OK
+             : DIT_ERR_CUDA;
+}
+
+dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v_new, void* k_buf,
+                                 void* v_buf, void* out, float* lse, int B, int H, int m, int N,
+                                 int D, int row0, float scale, dit_dtype out_dtype,
+                                 dit_stream stream) {
+  dit_status s = check_dims(B, H, N, D);
+  if (s != DIT_OK) return s;
+  if (m < 1 || row0 < 0 || row0 > N - m) return DIT_ERR_INVALID_ARG;
+  if (!k_new || !v_new || !k_buf || !v_buf) return DIT_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_buf, 16) || !aligned(v_buf, 16))
+    return DIT_ERR_INVALID_ARG;
+  // Attention arguments: m patch queries against the N rows of the (updated) buffer.
+  const long long hs = static_cast<long long>(N) * D;
+  s = validate_attention(q, k_buf, v_buf, out, lse, B, H, m, N, D, hs, scale, out_dtype);
+  if (s != DIT_OK) return s;
+  const long long bh = static_cast<long long>(B) * H;
+  const Range rkb = span(k_buf, bh * hs * 2), rvb = span(v_buf, bh * hs * 2);
+  const Range rkn = span(k_new, bh * m * D * 2), rvn = span(v_new, bh * m * D * 2);
+  const Range rq = span(q, bh * m * D * 2);
+  if (overlap(rkb, rvb)) return DIT_ERR_INVALID_ARG;
+  const Range ro = span(out, bh * m * D * dtype_bytes(out_dtype)), rl = span(lse, bh * m * 4);
+  for (Range buf : {rkb, rvb})
+    for (Range other : {rkn, rvn, rq})
+      if (overlap(buf, other)) return DIT_ERR_INVALID_ARG;
+  for (Range fresh : {rkn, rvn})
+    if (overlap(fresh, ro) || overlap(fresh, rl)) return DIT_ERR_INVALID_ARG;
+  if ((m + 63) / 64 > 65535) return DIT_ERR_UNSUPPORTED;  // copy grid (bf16, D <= 128)
+  // 1) fresh patch rows overwrite their stale rows, K and V in one launch
+  ditattn::CopyLaunch c;
+  c.src = k_new;
+  c.dst = static_cast<char*>(k_buf) + static_cast<long long>(row0) * D * 2;
+  c.src2 = v_new;
+  c.dst2 = static_cast<char*>(v_buf) + static_cast<long long>(row0) * D * 2;
+  c.ss = {static_cast<long long>(H) * m * D, static_cast<long long>(m) * D, D};
+  c.ds = {H * hs, hs, D};
+  c.batch = B;
+  c.heads = H;
+  c.n = m;
+  c.d = D;
+  c.elem_bytes = 2;
+  if (ditattn::launch_layout_copy(c, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DIT_ERR_CUDA;
+  // 2) the patch's queries against the whole buffer (fresh own rows, stale others)
+  return run_contiguous(q, k_buf, v_buf, out, lse, B, H, m, N, D, hs, scale, out_dtype, stream);
 }
 
 dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,

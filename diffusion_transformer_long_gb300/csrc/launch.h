@@ -6,19 +6,25 @@
 
 namespace ditattn {
 
+// Element strides of a logical [B, H, N, D] view: x[b][h][n][d] sits at
+// b * b_ + h * h_ + n * n_ + d elements from the base.
+struct Strides {
+  long long b_, h_, n_;
+};
+
 struct AttnLaunch {
   const void* q;
   const void* k;
   const void* v;
   void* out;
-  float* lse;
+  float* lse;                // contiguous [B, H, N_q]
   int* status;               // device status word
-  int bh;                    // B * H
+  int batch;                 // B
+  int heads;                 // H
   int n_q;
   int n_kv;
   int d;                     // 64 or 128
-  long long q_head_stride;   // elements
-  long long kv_head_stride;  // elements
+  Strides qs, ks, vs, os;    // views of q, k, v (bf16) and out
   float scale;
   bool out_f32;
   // Ring-hop accumulate: out (fp32) and lse hold a running (O, lse) that this pass
@@ -43,6 +49,19 @@ struct MergeLaunch {
 };
 
 cudaError_t launch_merge(const MergeLaunch& a, cudaStream_t st);
+
+struct CopyLaunch {
+  const void* src;
+  void* dst;
+  const void* src2 = nullptr;  // optional second pair with the same shape and strides
+  void* dst2 = nullptr;
+  Strides ss, ds;   // element strides of the two [B, H, N, D] views
+  int batch, heads, n, d;
+  int elem_bytes;   // 2 (bf16) or 4 (fp32); d * elem_bytes / 16 in {8, 16, 32}
+};
+
+// Row-vectorised strided copy between two views (the layout-copy kernel).
+cudaError_t launch_layout_copy(const CopyLaunch& a, cudaStream_t st);
 
 // Test-only failure injection behind dit_test_inject_stall.
 void set_stall_injection(int enable, long long wait_limit_cycles);

@@ -19,9 +19,16 @@ from . import build as _build
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
 DIT_F32, DIT_BF16 = 0, 1
 
-EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_chunk_fwd", "dit_attn_chunk_fwd_accumulate",
-                    "dit_attn_lse_merge", "dit_attn_check", "dit_test_inject_stall",
-                    "dit_test_set_grid_limit", "dit_status_string", "dit_version")
+EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_fwd_strided", "dit_attn_chunk_fwd",
+                    "dit_attn_chunk_fwd_accumulate", "dit_attn_lse_merge", "dit_layout_copy",
+                    "dit_attn_stale_kv_fwd",
+                    "dit_attn_check", "dit_test_inject_stall", "dit_test_set_grid_limit",
+                    "dit_status_string", "dit_version")
+
+
+class Strides(ctypes.Structure):
+    """dit_strides: element strides (b, h, n) of a [B, H, N, D] view with contiguous D."""
+    _fields_ = [("b", ctypes.c_longlong), ("h", ctypes.c_longlong), ("n", ctypes.c_longlong)]
 
 _lib = None
 
@@ -48,6 +55,13 @@ def lib() -> ctypes.CDLL:
         P, I, LL, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
         L.dit_attn_fwd.restype = I
         L.dit_attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
+        SP = ctypes.POINTER(Strides)
+        L.dit_attn_fwd_strided.restype = I
+        L.dit_attn_fwd_strided.argtypes = [P, SP, P, SP, P, SP, P, SP, P, I, I, I, I, I, F, I, P]
+        L.dit_attn_stale_kv_fwd.restype = I
+        L.dit_attn_stale_kv_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        L.dit_layout_copy.restype = I
+        L.dit_layout_copy.argtypes = [P, SP, P, SP, I, I, I, I, I, P]
         L.dit_attn_chunk_fwd.restype = I
         L.dit_attn_chunk_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, P]
         L.dit_attn_chunk_fwd_accumulate.restype = I
@@ -120,6 +134,136 @@ def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, s
                                 scale, _dt(out.dtype), _stream(q.device, stream))
     if st != DIT_OK:
         raise DitError(st, "dit_attn_fwd")
+    return out, lse
+
+
+def view_strides(x: torch.Tensor) -> Strides:
+    """dit_strides of a [B, H, N, D] tensor view whose last dimension is contiguous (e.g. a
+    token-major [B, N, H, D] tensor passed as x.transpose(1, 2))."""
+    if x.dim() != 4 or x.stride(3) != 1:
+        raise ValueError("expected a [B, H, N, D] view with contiguous last dimension")
+    return Strides(*(int(s) for s in x.stride()[:3]))
+
+
+def attn_fwd_strided(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32,
+                     stream=None):
+    """Attention over arbitrary strided [B, H, N, D] views (last dimension contiguous): q is
+    [B, H, N_q, D], k and v [B, H, n_kv, D].  A BSND tensor x ([B, N, H, D] in memory) is passed as
+    x.transpose(1, 2), and `out` may be such a view too.  Returns (out, lse fp32 [B, H, N_q])."""
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("q, k, v must be 4-D bf16 CUDA tensor views")
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v must be [B, H, n_kv, D] matching q")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
+    if tuple(out.shape) != (B, H, Nq, D):
+        raise ValueError("out must be a [B, H, N_q, D] view")
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    qs, ks, vs, os_ = (view_strides(t) for t in (q, k, v, out))
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_fwd_strided(_ptr(q), ctypes.byref(qs), _ptr(k), ctypes.byref(ks),
+                                        _ptr(v), ctypes.byref(vs), _ptr(out), ctypes.byref(os_),
+                                        _ptr(lse), B, H, Nq, k.shape[2], D, scale, _dt(out.dtype),
+                                        _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_fwd_strided")
+    return out, lse
+
+
+def layout_copy(src, dst, stream=None):
+    """dst[...] = src[...] for two [B, H, N, D] views of the same shape and dtype (bf16 or fp32,
+    last dimension contiguous), by the library's strided copy kernel.  Returns dst."""
+    if not (src.is_cuda and dst.is_cuda) or src.device != dst.device:
+        raise ValueError("src and dst must be CUDA tensors on one device")
+    if src.shape != dst.shape or src.dtype != dst.dtype or src.dim() != 4:
+        raise ValueError("src and dst must be [B, H, N, D] views of one shape and dtype")
+    B, H, N, D = src.shape
+    ss, ds = view_strides(src), view_strides(dst)
+    with torch.cuda.device(src.device):
+        st = lib().dit_layout_copy(_ptr(src), ctypes.byref(ss), _ptr(dst), ctypes.byref(ds), B, H,
+                                   N, D, _dt(src.dtype), _stream(src.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_layout_copy")
+    return dst
+
+
+def bsnd_to_bhnd(x, out=None, stream=None):
+    """Token-major [B, N, H, D] -> contiguous head-major [B, H, N, D]."""
+    B, N, H, D = x.shape
+    if out is None:
+        out = torch.empty((B, H, N, D), device=x.device, dtype=x.dtype)
+    layout_copy(x.transpose(1, 2), out, stream=stream)
+    return out
+
+
+def bhnd_to_bsnd(x, out=None, stream=None):
+    """Head-major [B, H, N, D] -> contiguous token-major [B, N, H, D]."""
+    B, H, N, D = x.shape
+    if out is None:
+        out = torch.empty((B, N, H, D), device=x.device, dtype=x.dtype)
+    layout_copy(x, out.transpose(1, 2), stream=stream)
+    return out
+
+
+def ulysses_pack(x_local, p, out=None, stream=None):
+    """Send buffers of one rank's Ulysses all-to-all: its token shard x_local [B, N/p, H, D]
+    (token-major) split by head groups into out [p, B, N/p, H/p, D], out[r] = the heads
+    r*H/p .. (r+1)*H/p that rank r will own.  One strided copy per destination rank."""
+    B, n, H, D = x_local.shape
+    if H % p:
+        raise ValueError("Ulysses needs the head count divisible by the degree")
+    hp = H // p
+    if out is None:
+        out = torch.empty((p, B, n, hp, D), device=x_local.device, dtype=x_local.dtype)
+    for r in range(p):
+        layout_copy(x_local[:, :, r * hp:(r + 1) * hp].transpose(1, 2), out[r].transpose(1, 2),
+                    stream=stream)
+    return out
+
+
+def ulysses_unpack(recv, out=None, stream=None):
+    """Receive side: recv [p, B, N/p, H/p, D], recv[r] = the token shard of rank r for this
+    rank's head group, assembled into all tokens of those heads, out [B, N, H/p, D]
+    (token-major; pass out.transpose(1, 2) to the attention as a [B, H/p, N, D] view)."""
+    p, B, n, hp, D = recv.shape
+    if out is None:
+        out = torch.empty((B, p * n, hp, D), device=recv.device, dtype=recv.dtype)
+    for r in range(p):
+        layout_copy(recv[r].transpose(1, 2), out[:, r * n:(r + 1) * n].transpose(1, 2),
+                    stream=stream)
+    return out
+
+
+def stale_kv_attention(q, k_new, v_new, k_buf, v_buf, row0, out=None, lse=None, scale=None,
+                       out_dtype=torch.float32, stream=None):
+    """One patch of displaced patch parallelism: the patch's fresh K/V rows [row0, row0 + m)
+    overwrite their stale rows of the KV buffers (in place), then its m queries attend to all N
+    buffer rows.  q, k_new, v_new [B, H, m, D]; k_buf, v_buf [B, H, N, D]; all bf16, contiguous.
+    Returns (out [B, H, m, D], lse fp32 [B, H, m])."""
+    for t in (q, k_new, v_new, k_buf, v_buf):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError("q, k_new, v_new, k_buf, v_buf must be contiguous 4-D bf16 CUDA tensors")
+    B, H, m, D = q.shape
+    N = k_buf.shape[2]
+    if k_new.shape != q.shape or v_new.shape != q.shape or v_buf.shape != k_buf.shape \
+            or tuple(k_buf.shape[:2]) != (B, H) or k_buf.shape[3] != D:
+        raise ValueError("shape mismatch between the patch and the KV buffers")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, m, D), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, m), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_stale_kv_fwd(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_buf),
+                                         _ptr(v_buf), _ptr(out), _ptr(lse), B, H, m, N, D,
+                                         int(row0), scale, _dt(out.dtype),
+                                         _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_stale_kv_fwd")
     return out, lse
 
 

@@ -51,6 +51,15 @@ typedef enum { DIT_F32 = 0, DIT_BF16 = 1 } dit_dtype;
 /* Opaque CUDA stream (cudaStream_t / CUstream). */
 typedef void* dit_stream;
 
+/* Element strides of a logical [B, H, N, D] view whose last dimension is
+ * contiguous: with s = the strides, element (i_b, i_h, i_n, i_d) sits
+ * i_b*s.b + i_h*s.h + i_n*s.n + i_d elements from the base.  Contiguous BHND
+ * is {H*N*D, N*D, D}; the token-major BSND layout ([B, N, H, D] in memory) is
+ * {N*H*D, D, H*D}. */
+typedef struct {
+  long long b, h, n;
+} dit_strides;
+
 /*
  * Fused attention over all N keys.
  * Defines: per head, s_ij = scale * q_i . k_j; o_i = sum_j softmax_j(s_ij) v_j;
@@ -90,6 +99,28 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
                               dit_stream stream);
 
 /*
+ * General-layout form of dit_attn_fwd / dit_attn_chunk_fwd: attention of N_q
+ * queries against n_kv keys, each of q, k, v and out an arbitrary strided
+ * [B, H, N, D] view (last dimension contiguous).  This reads and writes the
+ * token-major BSND layout in which the pages' sequence-parallel code keeps its
+ * activations (the MindIE-SD parallelism docs run their attention kernel on
+ * BSND tensors; valdrada.cn Wan2.2, CP section: tokens are split across ranks
+ * and heads kept whole) directly, with no transpose.
+ *   q, k, v     : device bf16 views; NULL strides = contiguous BHND
+ *   out         : device view of out_dtype (written); NULL strides = contiguous
+ *   lse         : device fp32 [B, H, N_q], contiguous (written)
+ * Strides must be positive multiples of 8 elements (16-byte TMA strides) below
+ * 2^39; out must not map two elements to one address; out and lse must not
+ * overlap the address range of q, k or v (DIT_ERR_INVALID_ARG otherwise).
+ */
+dit_status dit_attn_fwd_strided(const void* q, const dit_strides* q_strides, const void* k,
+                                const dit_strides* k_strides, const void* v,
+                                const dit_strides* v_strides, void* out,
+                                const dit_strides* out_strides, float* lse, int B, int H, int N_q,
+                                int n_kv, int D, float scale, dit_dtype out_dtype,
+                                dit_stream stream);
+
+/*
  * One Ring-attention hop with the merge fused into the chunk pass: the attention
  * of all N_q queries against ONE KV chunk, (O_c, lse_c) exactly as
  * dit_attn_chunk_fwd defines them, is merged in place into a running output:
@@ -127,6 +158,46 @@ dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const voi
 dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,
                               float* lse, int B, int H, int N, int D, dit_dtype partial_dtype,
                               dit_dtype out_dtype, dit_stream stream);
+
+/*
+ * Stale-KV attention of one patch, as displaced patch parallelism runs it
+ * (PipeFusion / DistriFusion: arganzheng.life multi-GPU diffusion parallelism,
+ * section 6 PipeFusion; xllm-io review of PipeFusion, method section; TACO-DiT,
+ * hybrid SP KV buffer): a KV buffer holds K, V of all N tokens from the previous
+ * diffusion step; the patch's freshly computed K, V rows [row0, row0 + m)
+ * overwrite their stale rows in place, then the patch's m queries attend to the
+ * whole buffer (their own rows fresh, every other row stale).  Two launches on
+ * `stream`: the row update (K and V together), then the attention.
+ *   q            : device bf16 [B, H, m, D] (the patch's queries), contiguous
+ *   k_new, v_new : device bf16 [B, H, m, D], contiguous (read)
+ *   k_buf, v_buf : device bf16 [B, H, N, D], contiguous (rows [row0, row0+m)
+ *                  overwritten, then read)
+ *   out, lse     : as dit_attn_chunk_fwd for N_q = m queries over n_kv = N keys
+ * 0 <= row0 <= N - m; the buffers must not overlap each other or q, k_new, v_new.
+ */
+dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v_new, void* k_buf,
+                                 void* v_buf, void* out, float* lse, int B, int H, int m, int N,
+                                 int D, int row0, float scale, dit_dtype out_dtype,
+                                 dit_stream stream);
+
+/*
+ * Copies a logical [B, H, N, D] tensor of `dtype` elements from one strided
+ * view to another (last dimension contiguous in both).  This is the local, on-GPU
+ * half of Ulysses sequence parallelism's re-shard around attention, where an
+ * all-to-all turns each rank's token shard of all heads into all tokens of its
+ * head shard (arganzheng.life multi-GPU diffusion parallelism, section 4.1
+ * Ulysses; valdrada.cn Wan2.2, CP section): the token-major (BSND) <-> head-major
+ * (BHND) transpose and the packing of per-rank send buffers are such copies, and
+ * so is writing fresh K/V rows into a KV buffer in place (a row-range view as dst).
+ *   src, dst     : device pointers, 16-byte aligned; NULL strides = contiguous BHND
+ *   D            : 64 or 128 (else DIT_ERR_UNSUPPORTED)
+ * Strides follow dit_attn_fwd_strided's rules; dst must not map two elements to
+ * one address and the two views' address ranges must not overlap
+ * (DIT_ERR_INVALID_ARG).  Bit-exact: values are moved, never converted.
+ */
+dit_status dit_layout_copy(const void* src, const dit_strides* src_strides, void* dst,
+                           const dit_strides* dst_strides, int B, int H, int N, int D,
+                           dit_dtype dtype, dit_stream stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device status

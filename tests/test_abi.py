@@ -130,6 +130,76 @@ def test_accumulate_binding_checks_running_state(lib):
         da.ring_attention(x, x, x, [3, 4])
 
 
+def strided(lib, qs=None, ks=None, vs=None, os_=None, out=OUT, B=2, H=3, N=256, n_kv=100, D=128,
+            dt=0):
+    def ref(x):
+        return None if x is None else ctypes.byref(da.Strides(*x))
+    return lib.dit_attn_fwd_strided(Q, ref(qs), K, ref(ks), V, ref(vs), out, ref(os_), LSE, B, H, N,
+                                    n_kv, D, 0.088, dt, None)
+
+
+BSND = (256 * 3 * 128, 128, 3 * 128)  # [B, N, H, D] memory, B=2 H=3 N=256 D=128
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qs=(0, 128, 384)), da.DIT_ERR_INVALID_ARG),                 # zero stride
+    (dict(ks=(-8, 128, 384)), da.DIT_ERR_INVALID_ARG),                # negative stride
+    (dict(vs=(98304, 132, 384)), da.DIT_ERR_INVALID_ARG),             # not a multiple of 8
+    (dict(qs=(1 << 39, 128, 384)), da.DIT_ERR_INVALID_ARG),
+    (dict(os_=(98304, 128, 64)), da.DIT_ERR_INVALID_ARG),             # out rows overlap
+    (dict(os_=(256 * 128, 128, 3 * 128)), da.DIT_ERR_INVALID_ARG),   # out batches overlap
+    (dict(out=ctypes.c_void_p((1 << 40) + 256)), da.DIT_ERR_INVALID_ARG),  # out inside q's range
+    (dict(D=96), da.DIT_ERR_UNSUPPORTED), (dict(n_kv=0), da.DIT_ERR_INVALID_ARG),
+    (dict(dt=5), da.DIT_ERR_INVALID_ARG),
+])
+def test_strided_validation(lib, kw, status):
+    assert strided(lib, **kw) == status
+
+
+def test_strided_size_one_dimensions_take_any_stride(lib):
+    # B = 1, H = 1: their strides address nothing; validation must not reject them (the call
+    # then fails only at launch, here without a GPU).
+    st = strided(lib, qs=(0, 3, 128), ks=(0, 1, 128), vs=(5, 5, 128), os_=(0, 0, 128), B=1, H=1)
+    assert st not in (da.DIT_ERR_INVALID_ARG, da.DIT_ERR_UNSUPPORTED)
+
+
+def copy(lib, src=Q, ss=None, dst=OUT, ds=None, B=2, H=3, N=256, D=128, dt=1):
+    def ref(x):
+        return None if x is None else ctypes.byref(da.Strides(*x))
+    return lib.dit_layout_copy(src, ref(ss), dst, ref(ds), B, H, N, D, dt, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(src=None), da.DIT_ERR_INVALID_ARG), (dict(N=0), da.DIT_ERR_INVALID_ARG),
+    (dict(D=32), da.DIT_ERR_UNSUPPORTED), (dict(dt=9), da.DIT_ERR_INVALID_ARG),
+    (dict(dst=ctypes.c_void_p((4 << 40) + 8)), da.DIT_ERR_INVALID_ARG),
+    (dict(ss=(1, 128, 384)), da.DIT_ERR_INVALID_ARG),
+    (dict(ds=(98304, 128, 64)), da.DIT_ERR_INVALID_ARG),               # dst rows overlap
+    (dict(dst=ctypes.c_void_p((1 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),  # dst inside src
+    (dict(N=70000 * 64), da.DIT_ERR_UNSUPPORTED),                      # copy grid too tall
+])
+def test_layout_copy_validation(lib, kw, status):
+    assert copy(lib, **kw) == status
+
+
+def stale(lib, q=Q, kn=K, vn=V, kb=ctypes.c_void_p(6 << 40), vb=ctypes.c_void_p(7 << 40), out=OUT,
+          lse=LSE, B=1, H=2, m=256, N=1024, D=128, row0=256):
+    return lib.dit_attn_stale_kv_fwd(q, kn, vn, kb, vb, out, lse, B, H, m, N, D, row0, 0.088, 0, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=0), da.DIT_ERR_INVALID_ARG), (dict(row0=-1), da.DIT_ERR_INVALID_ARG),
+    (dict(row0=769), da.DIT_ERR_INVALID_ARG),                          # patch past the buffer
+    (dict(m=1025), da.DIT_ERR_INVALID_ARG), (dict(D=80), da.DIT_ERR_UNSUPPORTED),
+    (dict(kn=None), da.DIT_ERR_INVALID_ARG),
+    (dict(kb=ctypes.c_void_p((7 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),   # k_buf inside v_buf
+    (dict(kn=ctypes.c_void_p((6 << 40) + 1024)), da.DIT_ERR_INVALID_ARG),   # k_new inside k_buf
+    (dict(out=ctypes.c_void_p((2 << 40) + 64)), da.DIT_ERR_INVALID_ARG),    # out inside k_new
+])
+def test_stale_kv_validation(lib, kw, status):
+    assert stale(lib, **kw) == status
+
+
 def merge(lib, p=4, parts=Q, lses=K, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, pdt=0, odt=0):
     return lib.dit_attn_lse_merge(parts, lses, p, out, lse, B, H, N, D, pdt, odt, None)
 
