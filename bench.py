@@ -561,6 +561,44 @@ def run_gpu(args):
     return 0
 
 
+def run_profile_case(args):
+    """Runs ONE path of the step (--warmup + --steps launches, untimed, no JSON) on the
+    workload's inputs and nothing else: the small, short command an ncu capture wraps."""
+    from diffusion_transformer_long_gb300 import ditattn as da
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    q, k, v = (t.to(dev) for t in synth.make_qkv(w))
+    B, H, N, D, p = w.B, w.H, w.N, w.D, w.p
+    out = torch.empty((B, H, N, D), device=dev, dtype=torch.float32)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    s0, n0 = synth.chunk_starts(w.chunks)[1], w.chunks[1]
+    if args.profile_case == "merge":
+        parts = torch.randn((p, B, H, N, D), device=dev)
+        lses = torch.randn((p, B, H, N), device=dev)
+    if args.profile_case == "transpose":
+        src = da.bhnd_to_bsnd(q)
+        dst = torch.empty_like(q)
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup + args.steps):
+        if args.profile_case == "fused":
+            da.attn_fwd(q, k, v, out=out, lse=lse, scale=w.scale)
+        elif args.profile_case == "chunk":
+            da.attn_chunk_fwd(q, k[:, :, s0:s0 + n0], v[:, :, s0:s0 + n0], out=out, lse=lse,
+                              scale=w.scale)
+        elif args.profile_case == "accumulate":
+            da.attn_chunk_fwd_accumulate(q, k[:, :, s0:s0 + n0], v[:, :, s0:s0 + n0], out, lse,
+                                         scale=w.scale)
+        elif args.profile_case == "merge":
+            da.attn_lse_merge(parts, lses, out=out, lse=lse)
+        elif args.profile_case == "transpose":
+            da.bsnd_to_bhnd(src, out=dst)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,6 +609,8 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["fused", "chunk", "accumulate", "merge", "transpose"],
+                    help="run only this path, untimed (for ncu captures); prints nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -579,6 +619,8 @@ def main(argv=None):
     if not torch.cuda.is_available():
         print(json.dumps({"error": "no CUDA device"}))
         return 1
+    if args.profile_case:
+        return run_profile_case(args)
     return run_gpu(args)
 
 
