@@ -418,22 +418,28 @@ def run_gpu(args):
     k_new, v_new = k[:, :, :m].contiguous(), v[:, :, :m].contiguous()
     o_patch = torch.empty((B, H, m, D), device=dev, dtype=torch.float32)
     l_patch = torch.empty((B, H, m), device=dev, dtype=torch.float32)
-    for _ in range(args.warmup):
-        da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
-                              scale=w.scale)
-    torch.cuda.synchronize(dev)
-    st_0, st_1 = ev(), ev()
-    ns = max(5, args.steps)
-    st_0.record(stream)
-    for _ in range(ns):
-        da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
-                              scale=w.scale)
-    st_1.record(stream)
-    torch.cuda.synchronize(dev)
-    da.check(dev)
-    stale_ms = max_over_ranks(dist, st_0.elapsed_time(st_1) / ns)
+    s_split, ws = da.splitkv_plan(B, H, m, N, D, dev)  # the library's split-KV suggestion
+
+    def stale_ms_for(splits):
+        for _ in range(args.warmup):
+            da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
+                                  scale=w.scale, splits=splits, workspace=ws)
+        torch.cuda.synchronize(dev)
+        st_0, st_1 = ev(), ev()
+        ns = max(5, args.steps)
+        st_0.record(stream)
+        for _ in range(ns):
+            da.stale_kv_attention(q_patch, k_new, v_new, kb, vb, 0, out=o_patch, lse=l_patch,
+                                  scale=w.scale, splits=splits, workspace=ws)
+        st_1.record(stream)
+        torch.cuda.synchronize(dev)
+        da.check(dev)
+        return max_over_ranks(dist, st_0.elapsed_time(st_1) / ns)
+
+    stale_ms = stale_ms_for(s_split)
+    stale_ms_unsplit = stale_ms_for(1)
     stale_flops = 4.0 * B * H * m * N * D
-    del kb, vb, q_patch, k_new, v_new, o_patch, l_patch
+    del kb, vb, q_patch, k_new, v_new, o_patch, l_patch, ws
 
     # ---- cross-attention shape: all N queries against 512 replicated text keys ----
     n_txt = 512
@@ -535,8 +541,11 @@ def run_gpu(args):
                                            "gbs": transpose_bytes / (transpose_ms * 1e-3) / 1e9,
                                            "frac_of_hbm": transpose_bytes / (transpose_ms * 1e-3)
                                            / 1e9 / hbm},
-                "stale_kv_patch": {"ms": stale_ms, "queries": m, "keys": N,
-                                   "tflops": stale_flops / (stale_ms * 1e-3) / 1e12},
+                "stale_kv_patch": {"ms": stale_ms, "queries": m, "keys": N, "kv_splits": s_split,
+                                   "tflops": stale_flops / (stale_ms * 1e-3) / 1e12,
+                                   "unsplit_ms": stale_ms_unsplit,
+                                   "unsplit_tflops": stale_flops / (stale_ms_unsplit * 1e-3)
+                                   / 1e12},
                 "cross_attention_512_text_keys": {"ms": cross_ms,
                                                   "tflops": cross_flops / (cross_ms * 1e-3) / 1e12},
                 "fused_vs_chunk_max_abs": diff,

@@ -92,31 +92,59 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
       !encode_view(&prm.tm_k, a.k, a.d, a.n_kv, a.heads, a.batch, a.ks) ||
       !encode_view(&prm.tm_v, a.v, a.d, a.n_kv, a.heads, a.batch, a.vs))
     return cudaErrorInvalidValue;
-  prm.out_f32 = a.out_f32 ? static_cast<float*>(a.out) : nullptr;
-  prm.out_bf16 = a.out_f32 ? nullptr : static_cast<__nv_bfloat16*>(a.out);
-  prm.o_sb = a.os.b_;
-  prm.o_sh = a.os.h_;
-  prm.o_sn = a.os.n_;
+  const bool split = a.splits > 1;
+  if (split && (a.accumulate || !a.ws_o || !a.ws_lse)) return cudaErrorInvalidValue;
+  // Split-KV passes write fp32 partials, contiguous, into the workspace.
+  const bool f32 = split || a.out_f32;
+  void* const obase = split ? static_cast<void*>(a.ws_o) : a.out;
+  const Strides os = split ? Strides{static_cast<long long>(a.heads) * a.n_q * a.d,
+                                     static_cast<long long>(a.n_q) * a.d, a.d}
+                           : a.os;
+  prm.out_f32 = f32 ? static_cast<float*>(obase) : nullptr;
+  prm.out_bf16 = f32 ? nullptr : static_cast<__nv_bfloat16*>(obase);
+  prm.o_sb = os.b_;
+  prm.o_sh = os.h_;
+  prm.o_sn = os.n_;
   // 32-byte row segments need the base and every stride (in bytes) 32-byte aligned.
-  const long long esize = a.out_f32 ? 4 : 2;
-  prm.out_align32 = (reinterpret_cast<uintptr_t>(a.out) % 32 == 0 && (a.os.b_ * esize) % 32 == 0 &&
-                     (a.os.h_ * esize) % 32 == 0 && (a.os.n_ * esize) % 32 == 0)
+  const long long esize = f32 ? 4 : 2;
+  prm.out_align32 = (reinterpret_cast<uintptr_t>(obase) % 32 == 0 && (os.b_ * esize) % 32 == 0 &&
+                     (os.h_ * esize) % 32 == 0 && (os.n_ * esize) % 32 == 0)
                         ? 1
                         : 0;
-  prm.lse = a.lse;
+  prm.lse = split ? a.ws_lse : a.lse;
   prm.status = a.status;
   prm.n_q = a.n_q;
   prm.n_kv = a.n_kv;
   prm.bh_count = a.batch * a.heads;
   prm.heads = a.heads;
   prm.q_pairs = (a.n_q + 2 * kBlockM - 1) / (2 * kBlockM);
-  prm.num_items = prm.q_pairs * prm.bh_count;
+  prm.splits = split ? a.splits : 1;
+  prm.tiles_total = (a.n_kv + kBlockN - 1) / kBlockN;
+  const long long rows = static_cast<long long>(prm.bh_count) * a.n_q;
+  prm.ws_o_stride = split ? rows * a.d : 0;
+  prm.ws_l_stride = split ? rows : 0;
+  prm.num_items = prm.q_pairs * prm.bh_count * prm.splits;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;
   prm.stall_kv = g_stall_kv;
   if (a.accumulate) {
     if (!a.out_f32) return cudaErrorInvalidValue;
     return a.d == 64 ? launch_typed<64, true, true>(prm, st) : launch_typed<128, true, true>(prm, st);
+  }
+  if (split) {
+    const cudaError_t e = a.d == 64 ? launch_typed<64, true>(prm, st) : launch_typed<128, true>(prm, st);
+    if (e != cudaSuccess) return e;
+    MergeLaunch m;
+    m.partials = a.ws_o;
+    m.lses = a.ws_lse;
+    m.p = a.splits;
+    m.rows = rows;
+    m.d = a.d;
+    m.out = a.out;
+    m.lse = a.lse;
+    m.part_f32 = true;
+    m.out_f32 = a.out_f32;
+    return launch_merge(m, st);
   }
   if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
   return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);

@@ -93,12 +93,11 @@ constexpr int kPvWarp = 10;     // O += P V issuer
 constexpr int kEpiWarp0 = 12;   // warps 12-15: epilogue warpgroup
 // Register split (setmaxnreg): 512 threads launch with 128 registers each (65536);
 // softmax warpgroups grow to 176, the producer/issuer warpgroup shrinks to 72 and
-// the epilogue warpgroup to 80: 2*128*176 + 128*72 + 128*80 = 64512 <= 65536, and
-// per SM sub-partition (one warp of each warpgroup) 176+176+72+80 = 504 <= 512.
+// the epilogue warpgroup to 88: 2*128*176 + 128*72 + 128*88 = 65536, and per SM
+// sub-partition (one warp of each warpgroup) 176+176+72+88 = 512.
 constexpr uint32_t kRegsSoftmax = 176;
 constexpr uint32_t kRegsIssue = 72;
-constexpr uint32_t kRegsEpilogue = 80;
-constexpr uint32_t kRegsEpilogueAccum = 88;  // 2*128*176 + 128*72 + 128*88 = 65536
+constexpr uint32_t kRegsEpilogue = 88;
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
@@ -118,7 +117,11 @@ struct AttnParams {
   int bh_count;
   int heads;          // H: head bh is (b, h) = (bh / H, bh % H)
   int q_pairs;        // ceil(n_q / 256)
-  int num_items;      // bh_count * q_pairs
+  int splits;         // key ranges per (head, Q pair): 1, or S for split-KV partials
+  int tiles_total;    // ceil(n_kv / 128)
+  long long ws_o_stride;  // split-KV: elements between consecutive splits' partial O (else 0)
+  long long ws_l_stride;  // split-KV: elements between consecutive splits' partial LSEs (else 0)
+  int num_items;      // bh_count * q_pairs * splits
   float scale_log2;   // scale * log2(e)
   long long wait_limit;  // SM clocks a bounded wait may spin before giving up
   int stall_kv;          // test-only failure injection: never issue K/V copies
@@ -183,14 +186,27 @@ struct Item {
   int bh;      // b * H + h
   int b, h;
   int q_row0;  // first query row of the pair of Q tiles
+  int split;   // key range of the item (0 unless split-KV)
+  int tile0;   // first KV tile of the range
+  int ntiles;  // KV tiles in the range (>= 1)
   __device__ __forceinline__ size_t out_off(const AttnParams& p) const {
-    return static_cast<size_t>(b) * p.o_sb + static_cast<size_t>(h) * p.o_sh;
+    return static_cast<size_t>(b) * p.o_sb + static_cast<size_t>(h) * p.o_sh +
+           static_cast<size_t>(split) * p.ws_o_stride;
+  }
+  __device__ __forceinline__ size_t lse_off(const AttnParams& p) const {
+    return static_cast<size_t>(bh) * p.n_q + static_cast<size_t>(split) * p.ws_l_stride;
   }
 };
+// Work item w: (head, Q pair, key range), key range fastest.  Split s of S covers KV tiles
+// [s*T/S, (s+1)*T/S) of the T tiles.
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
-  const int bh = w / p.q_pairs;
+  const int qi = w / p.splits;
+  const int split = w - qi * p.splits;
+  const int bh = qi / p.q_pairs;
   const int b = bh / p.heads;
-  return {bh, b, bh - b * p.heads, (w % p.q_pairs) * 2 * kBlockM};
+  const int tile0 = static_cast<int>(static_cast<long long>(split) * p.tiles_total / p.splits);
+  const int tile1 = static_cast<int>(static_cast<long long>(split + 1) * p.tiles_total / p.splits);
+  return {bh, b, bh - b * p.heads, (qi % p.q_pairs) * 2 * kBlockM, split, tile0, tile1 - tile0};
 }
 
 // K/V ring items of one work item, in consumption order: K_0, then per KV tile j:
@@ -204,7 +220,7 @@ __device__ __forceinline__ int v_item(int j, int n_tiles) {
 }
 
 template <int D>
-__device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, int n_tiles,
+__device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase,
                                          volatile int* abort_flag) {
   using L = AttnSmem<D>;
   constexpr int kRegions = D / 64;
@@ -264,10 +280,10 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase, in
     ++q_loads;
     if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
 
-    if (!(ok = load(false, 0, item))) break;
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      if (j + 1 < n_tiles && !(ok = load(false, j + 1, item))) break;
-      ok = load(true, j, item);
+    if (!(ok = load(false, item.tile0, item))) break;
+    for (int j = 0; ok && j < item.ntiles; ++j) {
+      if (j + 1 < item.ntiles && !(ok = load(false, item.tile0 + j + 1, item))) break;
+      ok = load(true, item.tile0 + j, item);
     }
   }
   if (!ok) {
@@ -318,7 +334,7 @@ struct Descs {
 // S_t = Q_t K^T for every KV tile of every work item (warp kMmaWarp, one thread).
 template <int D>
 __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
-                                         int n_tiles, volatile int* abort_flag) {
+                                         volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN, false, false);
@@ -344,7 +360,8 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
   int li = 0;         // work items started
   int ring0 = 0;      // ring index of this item's first K/V tile
   bool ok = true;
-  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li, ring0 += 2 * n_tiles) {
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
+    const int n_tiles = item_of(p, w).ntiles;
     if (!(ok = wait(L::bQFull, li & 1))) break;
     DIT_TRACE(kTrQFull, li);
     for (int j = 0; j < n_tiles; ++j, ++g) {
@@ -367,6 +384,7 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
       DIT_TRACE(kTrMmaS1, g);
     }
     if (ok) ptx::mma_commit(bar(L::bQEmpty));  // Q_0/Q_1 free once these MMAs are done
+    ring0 += 2 * n_tiles;
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -379,7 +397,7 @@ __device__ __forceinline__ void s_issuer(const AttnParams& p, uint32_t sbase, ui
 // O_t += P_t V_j for every KV tile of every work item (warp kPvWarp, one thread).
 template <int D>
 __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, uint32_t tmem,
-                                          int n_tiles, volatile int* abort_flag) {
+                                          volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, D, false, true);
@@ -404,7 +422,8 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
   int li = 0;
   int ring0 = 0;
   bool ok = true;
-  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li, ring0 += 2 * n_tiles) {
+  for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
+    const int n_tiles = item_of(p, w).ntiles;
     for (int j = 0; j < n_tiles; ++j, ++g) {
       const int sV = (ring0 + v_item(j, n_tiles)) % kStages;
       if (!(ok = wait(L::bPFull + 0, g & 1))) break;
@@ -428,6 +447,7 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
       ptx::mma_commit(bar(L::bKVEmpty + sV));
       DIT_TRACE(kTrMmaPv1, g);
     }
+    ring0 += 2 * n_tiles;
   }
   if (!ok) {
     raise_abort(p, abort_flag);
@@ -448,7 +468,7 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
 
 template <int D, bool kAccum>
 __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
-                                           int t, int warp, int lane, int n_tiles,
+                                           int t, int warp, int lane,
                                            volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
@@ -471,11 +491,18 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
   int li = 0;  // work items processed
   bool ok = true;
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
-    const Item item = item_of(p, w);
+    // Only the key range is live across the tile loop; the rest of the item is
+    // recomputed at its end.
+    int ntiles, kv_left;  // tiles of the item, keys from its first tile to n_kv
+    {
+      const Item it = item_of(p, w);
+      ntiles = it.ntiles;
+      kv_left = p.n_kv - it.tile0 * kBlockN;
+    }
     float m = -INFINITY;  // running max of scale*log2e*s (possibly stale by < 2^8)
     float l = 0.f;        // running sum of 2^(c*s - m), for the LSE
     float lp = 0.f;       // running sum of the bf16-rounded P the PV GEMM sees, for O
-    for (int j = 0; j < n_tiles; ++j, ++g) {
+    for (int j = 0; j < ntiles; ++j, ++g) {
       if (!(ok = wait(L::bSFull + t, g & 1))) break;
       if (r == 0) DIT_TRACE(kTrSmFull0 + 5 * t, g);
       if (r == 0 && t == 0 && g == 0) DIT_TRACE(kTrCta, 1);
@@ -499,7 +526,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       if (r == 0) DIT_TRACE(kTrSmLd0 + 5 * t, g);
 
       float mx = ptx::fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
-      const int valid = p.n_kv - j * kBlockN;
+      const int valid = kv_left - j * kBlockN;
       if (valid < kBlockN) {
         // Ragged last tile: keys past n_kv (zero-filled K rows) are masked to -inf and
         // the max is taken over the valid columns only.
@@ -605,8 +632,9 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     // sum to one; the LSE uses the unrounded sum.
     constexpr float kLn2 = 0.69314718055994530942f;
     const float lse2 = m + log2f(l);  // this pass's LSE in log2 units
+    const Item item = item_of(p, w);
     const int row = item.q_row0 + t * kBlockM + r;
-    float* const lse_row = p.lse + static_cast<size_t>(item.bh) * p.n_q + row;
+    float* const lse_row = p.lse + item.lse_off(p) + row;
     if constexpr (!kAccum) {
       // Slot [t][r] = 1 / lp, reused once the epilogue has taken the previous item's value.
       if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
@@ -678,7 +706,7 @@ __device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uin
 // faster there.
 template <int D, bool kOutF32, bool kAccum>
 __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
-                                            int warp, int lane, int n_tiles,
+                                            int warp, int lane,
                                             volatile int* abort_flag) {
   static_assert(kOutF32 || !kAccum, "the running output is fp32");
   using L = AttnSmem<D>;
@@ -694,11 +722,13 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
   };
 
   int li = 0;
+  int g_end = 0;  // KV tiles of the items so far (CTA-global)
   bool ok = true;
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
     const Item item = item_of(p, w);
-    const int g_last = (li + 1) * n_tiles - 1;  // CTA-global index of the item's last tile
-    const size_t head_row0 = static_cast<size_t>(item.bh) * p.n_q;  // LSE rows
+    g_end += item.ntiles;
+    const int g_last = g_end - 1;  // CTA-global index of the item's last tile
+    const size_t head_row0 = item.lse_off(p);  // LSE rows
     const size_t out_off = item.out_off(p);                           // output head
     // Accumulate mode: this item's running LSEs (read now, long before they are needed)
     // and its running-output rows brought into L2 while the item runs.
@@ -821,19 +851,16 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
 #pragma unroll
         for (int half = 0; half < D / 64; ++half) {
           uint32_t wd[32];  // 64 columns of this thread's row as bf16 pairs
-          {
-            uint32_t a[32], b[32];
-            ptx::tmem_ld32(tO + half * 64, a);
-            ptx::tmem_ld32(tO + half * 64 + 32, b);
-            ptx::tmem_wait_ld();
-            release_if(half == D / 64 - 1);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              wd[i] = ptx::pack_bf16x2(__uint_as_float(a[2 * i]) * inv_l,
-                                       __uint_as_float(a[2 * i + 1]) * inv_l);
-              wd[16 + i] = ptx::pack_bf16x2(__uint_as_float(b[2 * i]) * inv_l,
-                                            __uint_as_float(b[2 * i + 1]) * inv_l);
-            }
+          for (int c = 0; c < 2; ++c) {
+            uint32_t a[32];
+            ptx::tmem_ld32(tO + half * 64 + c * 32, a);
+            ptx::tmem_wait_ld();
+            release_if(half == D / 64 - 1 && c == 1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              wd[c * 16 + i] = ptx::pack_bf16x2(__uint_as_float(a[2 * i]) * inv_l,
+                                                __uint_as_float(a[2 * i + 1]) * inv_l);
           }
           if (row < p.n_q) {
 #pragma unroll
@@ -859,7 +886,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t sbase = ptx::smem_addr(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int n_tiles = (p.n_kv + kBlockN - 1) / kBlockN;
 
   if (threadIdx.x == 0) {
     auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
@@ -901,20 +927,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp < kLoadWarp) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    detail::softmax_wg<D, kAccum>(p, sbase, tmem, warp >> 2, warp, lane, n_tiles, abort_flag);
+    detail::softmax_wg<D, kAccum>(p, sbase, tmem, warp >> 2, warp, lane, abort_flag);
   } else if (warp < kEpiWarp0) {
     ptx::setmaxnreg_dec<kRegsIssue>();
     if (warp == kLoadWarp) {
-      if (lane == 0) detail::producer<D>(p, sbase, n_tiles, abort_flag);
+      if (lane == 0) detail::producer<D>(p, sbase, abort_flag);
     } else if (warp == kMmaWarp) {
-      if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+      if (lane == 0) detail::s_issuer<D>(p, sbase, tmem, abort_flag);
     } else if (warp == kPvWarp) {
-      if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, n_tiles, abort_flag);
+      if (lane == 0) detail::pv_issuer<D>(p, sbase, tmem, abort_flag);
     }
     __syncwarp();
   } else {
-    ptx::setmaxnreg_dec<kAccum ? kRegsEpilogueAccum : kRegsEpilogue>();
-    detail::epilogue_wg<D, kOutF32, kAccum>(p, sbase, tmem, warp, lane, n_tiles, abort_flag);
+    ptx::setmaxnreg_dec<kRegsEpilogue>();
+    detail::epilogue_wg<D, kOutF32, kAccum>(p, sbase, tmem, warp, lane, abort_flag);
   }
 
   ptx::tc_fence_before();

@@ -5,8 +5,10 @@
 
 #include <climits>
 #include <cmath>
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
+#include <initializer_list>
 #include <utility>
 
 #include "../../include/ditattn.h"
@@ -92,6 +94,15 @@ long long view_span(const dit_strides& s, long long B, long long H, long long N,
 
 dit_strides contiguous(long long H, long long N, long long D) { return {H * N * D, N * D, D}; }
 
+// Split-KV workspace: fp32 partial O [splits, rows, D], then (256-byte aligned) fp32 partial
+// LSEs [splits, rows].
+long long splitkv_lse_offset(long long rows, long long D, long long splits) {
+  return (splits * rows * D * 4 + 255) / 256 * 256;
+}
+long long splitkv_bytes(long long rows, long long D, long long splits) {
+  return splitkv_lse_offset(rows, D, splits) + splits * rows * 4;
+}
+
 // A strided view usable by the kernels: strides positive multiples of 8 elements (16-byte
 // TMA strides) below 2^39, and the view must fit 64-bit byte offsets comfortably.
 bool valid_strides(const dit_strides& s) {
@@ -121,7 +132,8 @@ bool no_self_overlap(const dit_strides& s, long long B, long long H, long long N
 dit_status run_attention(const void* q, const dit_strides& qs, const void* k, const dit_strides& ks,
                          const void* v, const dit_strides& vs, void* out, const dit_strides& os,
                          float* lse, int B, int H, int N_q, int n_kv, int D, float scale,
-                         dit_dtype out_dtype, dit_stream stream, bool accumulate = false) {
+                         dit_dtype out_dtype, dit_stream stream, bool accumulate = false,
+                         int splits = 1, void* workspace = nullptr) {
   int* status = status_ptr();
   if (!status) return DIT_ERR_CUDA;
   ditattn::AttnLaunch a;
@@ -143,6 +155,12 @@ dit_status run_attention(const void* q, const dit_strides& qs, const void* k, co
   a.scale = scale;
   a.out_f32 = out_dtype == DIT_F32;
   a.accumulate = accumulate;
+  a.splits = splits;
+  if (splits > 1) {
+    const long long rows = static_cast<long long>(B) * H * N_q;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + splitkv_lse_offset(rows, D, splits));
+  }
   return ditattn::launch_attention(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? DIT_OK
              : DIT_ERR_CUDA;
@@ -151,11 +169,29 @@ dit_status run_attention(const void* q, const dit_strides& qs, const void* k, co
 // Contiguous q/out, K/V heads kv_head_stride elements apart (the chunk form).
 dit_status run_contiguous(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                           int H, int N_q, int n_kv, int D, long long kv_head_stride, float scale,
-                          dit_dtype out_dtype, dit_stream stream, bool accumulate = false) {
+                          dit_dtype out_dtype, dit_stream stream, bool accumulate = false,
+                          int splits = 1, void* workspace = nullptr) {
   const dit_strides qs = contiguous(H, N_q, D);
   const dit_strides kvs = {H * kv_head_stride, kv_head_stride, D};
   return run_attention(q, qs, k, kvs, v, kvs, out, qs, lse, B, H, N_q, n_kv, D, scale, out_dtype,
-                       stream, accumulate);
+                       stream, accumulate, splits, workspace);
+}
+
+// Split-KV arguments: 1 <= splits <= min(64, KV tiles); with splits > 1 a 256-byte-aligned
+// workspace of at least dit_attn_splitkv_workspace_bytes that overlaps none of `others`.
+dit_status validate_splits(int splits, int n_kv, const void* workspace, size_t workspace_bytes,
+                           int B, int H, int N_q, int D, std::initializer_list<Range> others) {
+  const int tiles = (n_kv + 127) / 128;
+  if (splits < 1 || splits > 64 || splits > tiles) return DIT_ERR_INVALID_ARG;
+  if (splits == 1) return DIT_OK;
+  const long long rows = static_cast<long long>(B) * H * N_q;
+  const long long need = splitkv_bytes(rows, D, splits);
+  if (!workspace || !aligned(workspace, 256) || static_cast<long long>(workspace_bytes) < need)
+    return DIT_ERR_INVALID_ARG;
+  const Range rw = span(workspace, need);
+  for (Range o : others)
+    if (overlap(rw, o)) return DIT_ERR_INVALID_ARG;
+  return DIT_OK;
 }
 
 }  // namespace
@@ -273,8 +309,8 @@ dit_status dit_layout_copy(const void* src, const dit_strides* src_strides, void
 
 dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v_new, void* k_buf,
                                  void* v_buf, void* out, float* lse, int B, int H, int m, int N,
-                                 int D, int row0, float scale, dit_dtype out_dtype,
-                                 dit_stream stream) {
+                                 int D, int row0, float scale, dit_dtype out_dtype, int splits,
+                                 void* workspace, size_t workspace_bytes, dit_stream stream) {
   dit_status s = check_dims(B, H, N, D);
   if (s != DIT_OK) return s;
   if (m < 1 || row0 < 0 || row0 > N - m) return DIT_ERR_INVALID_ARG;
@@ -296,6 +332,9 @@ dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v
       if (overlap(buf, other)) return DIT_ERR_INVALID_ARG;
   for (Range fresh : {rkn, rvn})
     if (overlap(fresh, ro) || overlap(fresh, rl)) return DIT_ERR_INVALID_ARG;
+  s = validate_splits(splits, N, workspace, workspace_bytes, B, H, m, D,
+                      {rq, rkn, rvn, rkb, rvb, ro, rl});
+  if (s != DIT_OK) return s;
   if ((m + 63) / 64 > 65535) return DIT_ERR_UNSUPPORTED;  // copy grid (bf16, D <= 128)
   // 1) fresh patch rows overwrite their stale rows, K and V in one launch
   ditattn::CopyLaunch c;
@@ -313,7 +352,50 @@ dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v
   if (ditattn::launch_layout_copy(c, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return DIT_ERR_CUDA;
   // 2) the patch's queries against the whole buffer (fresh own rows, stale others)
-  return run_contiguous(q, k_buf, v_buf, out, lse, B, H, m, N, D, hs, scale, out_dtype, stream);
+  return run_contiguous(q, k_buf, v_buf, out, lse, B, H, m, N, D, hs, scale, out_dtype, stream,
+                        false, splits, workspace);
+}
+
+size_t dit_attn_splitkv_workspace_bytes(int B, int H, int N_q, int D, int splits) {
+  if (B < 1 || H < 1 || N_q < 1 || D < 1 || splits < 1) return 0;
+  if (splits == 1) return 0;
+  return static_cast<size_t>(splitkv_bytes(static_cast<long long>(B) * H * N_q, D, splits));
+}
+
+int dit_attn_splitkv_suggest(int B, int H, int N_q, int n_kv) {
+  if (B < 1 || H < 1 || N_q < 1 || n_kv < 1) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 1;
+  // Persistent grid: one CTA per SM walks the (head, Q pair) items.  Below about four waves
+  // the last partial wave idles a large share of the SMs; split the keys of every item so
+  // that there are about six waves, keeping at least 8 KV tiles per split.
+  const long long items = static_cast<long long>(B) * H * ((N_q + 255) / 256);
+  if (items >= 4LL * sms) return 1;
+  const long long tiles = (n_kv + 127) / 128;
+  long long s = (6LL * sms + items - 1) / items;
+  s = std::min<long long>(s, std::min<long long>(16, tiles / 8));
+  return s < 2 ? 1 : static_cast<int>(s);
+}
+
+dit_status dit_attn_chunk_fwd_splitkv(const void* q, const void* k, const void* v, void* out,
+                                      float* lse, int B, int H, int N_q, int n_kv, int D,
+                                      long long kv_head_stride, float scale, dit_dtype out_dtype,
+                                      int splits, void* workspace, size_t workspace_bytes,
+                                      dit_stream stream) {
+  dit_status s = validate_attention(q, k, v, out, lse, B, H, N_q, n_kv, D, kv_head_stride, scale,
+                                    out_dtype);
+  if (s != DIT_OK) return s;
+  const long long bh = static_cast<long long>(B) * H;
+  if (((N_q + 255) / 256) * bh * splits > INT_MAX) return DIT_ERR_INVALID_ARG;
+  const long long kv_bytes = ((bh - 1) * kv_head_stride + static_cast<long long>(n_kv) * D) * 2;
+  s = validate_splits(splits, n_kv, workspace, workspace_bytes, B, H, N_q, D,
+                      {span(q, bh * N_q * D * 2), span(k, kv_bytes), span(v, kv_bytes),
+                       span(out, bh * N_q * D * dtype_bytes(out_dtype)), span(lse, bh * N_q * 4)});
+  if (s != DIT_OK) return s;
+  return run_contiguous(q, k, v, out, lse, B, H, N_q, n_kv, D, kv_head_stride, scale, out_dtype,
+                        stream, false, splits, workspace);
 }
 
 dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,

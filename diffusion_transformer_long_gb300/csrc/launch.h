@@ -30,6 +30,12 @@ struct AttnLaunch {
   // Ring-hop accumulate: out (fp32) and lse hold a running (O, lse) that this pass
   // merges into in place.
   bool accumulate = false;
+  // Split-KV: each (head, Q pair) is split over `splits` key ranges whose fp32 partials
+  // go to ws_o [splits, B, H, N_q, D] and ws_lse [splits, B, H, N_q]; a merge launch
+  // then writes out (contiguous BHND) and lse.  splits == 1: no workspace.
+  int splits = 1;
+  float* ws_o = nullptr;
+  float* ws_lse = nullptr;
 };
 
 // Encodes the TMA descriptors and launches the attention kernel on `st`.

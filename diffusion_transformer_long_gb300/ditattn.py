@@ -21,7 +21,8 @@ DIT_F32, DIT_BF16 = 0, 1
 
 EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_fwd_strided", "dit_attn_chunk_fwd",
                     "dit_attn_chunk_fwd_accumulate", "dit_attn_lse_merge", "dit_layout_copy",
-                    "dit_attn_stale_kv_fwd",
+                    "dit_attn_stale_kv_fwd", "dit_attn_chunk_fwd_splitkv",
+                    "dit_attn_splitkv_workspace_bytes", "dit_attn_splitkv_suggest",
                     "dit_attn_check", "dit_test_inject_stall", "dit_test_set_grid_limit",
                     "dit_status_string", "dit_version")
 
@@ -59,7 +60,15 @@ def lib() -> ctypes.CDLL:
         L.dit_attn_fwd_strided.restype = I
         L.dit_attn_fwd_strided.argtypes = [P, SP, P, SP, P, SP, P, SP, P, I, I, I, I, I, F, I, P]
         L.dit_attn_stale_kv_fwd.restype = I
-        L.dit_attn_stale_kv_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        L.dit_attn_stale_kv_fwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P,
+                                            ctypes.c_size_t, P]
+        L.dit_attn_chunk_fwd_splitkv.restype = I
+        L.dit_attn_chunk_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, I, P,
+                                                 ctypes.c_size_t, P]
+        L.dit_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        L.dit_attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+        L.dit_attn_splitkv_suggest.restype = I
+        L.dit_attn_splitkv_suggest.argtypes = [I, I, I, I]
         L.dit_layout_copy.restype = I
         L.dit_layout_copy.argtypes = [P, SP, P, SP, I, I, I, I, I, P]
         L.dit_attn_chunk_fwd.restype = I
@@ -238,11 +247,56 @@ def ulysses_unpack(recv, out=None, stream=None):
     return out
 
 
+def splitkv_plan(B, H, n_q, n_kv, D, device, splits=None, workspace=None):
+    """(splits, workspace) for a split-KV call: the library's suggestion when splits is None,
+    and a fresh torch workspace of the required size unless one is given."""
+    with torch.cuda.device(device):
+        if splits is None:
+            splits = int(lib().dit_attn_splitkv_suggest(B, H, n_q, n_kv))
+        need = int(lib().dit_attn_splitkv_workspace_bytes(B, H, n_q, D, splits))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if need and (workspace.numel() * workspace.element_size() < need or not workspace.is_cuda):
+        raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
+    return splits, workspace
+
+
+def attn_chunk_fwd_splitkv(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32,
+                           splits=None, workspace=None, stream=None):
+    """dit_attn_chunk_fwd with each (head, Q pair) split over key ranges into fp32 partials in
+    `workspace` and merged (for few queries against many keys).  splits=None asks the library;
+    the workspace is allocated with torch unless given.  Returns (out, lse)."""
+    _check_qkv(q, k, v)
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v chunk must be [B, H, n_kv, D] matching q")
+    hs = kv_head_stride(k)
+    if kv_head_stride(v) != hs:
+        raise ValueError("k and v chunks must have the same head stride")
+    n_kv = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    splits, workspace = splitkv_plan(B, H, Nq, n_kv, D, q.device, splits, workspace)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_chunk_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                              Nq, n_kv, D, hs, scale, _dt(out.dtype), splits,
+                                              ws_ptr, ws_bytes, _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_chunk_fwd_splitkv")
+    return out, lse
+
+
 def stale_kv_attention(q, k_new, v_new, k_buf, v_buf, row0, out=None, lse=None, scale=None,
-                       out_dtype=torch.float32, stream=None):
+                       out_dtype=torch.float32, splits=1, workspace=None, stream=None):
     """One patch of displaced patch parallelism: the patch's fresh K/V rows [row0, row0 + m)
     overwrite their stale rows of the KV buffers (in place), then its m queries attend to all N
     buffer rows.  q, k_new, v_new [B, H, m, D]; k_buf, v_buf [B, H, N, D]; all bf16, contiguous.
+    splits: key ranges of the attention (1: none; None: the library's suggestion).
     Returns (out [B, H, m, D], lse fp32 [B, H, m])."""
     for t in (q, k_new, v_new, k_buf, v_buf):
         if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
@@ -257,11 +311,14 @@ def stale_kv_attention(q, k_new, v_new, k_buf, v_buf, row0, out=None, lse=None, 
         out = torch.empty((B, H, m, D), device=q.device, dtype=out_dtype)
     if lse is None:
         lse = torch.empty((B, H, m), device=q.device, dtype=torch.float32)
+    splits, workspace = splitkv_plan(B, H, m, N, D, q.device, splits, workspace)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     with torch.cuda.device(q.device):
         st = lib().dit_attn_stale_kv_fwd(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_buf),
                                          _ptr(v_buf), _ptr(out), _ptr(lse), B, H, m, N, D,
-                                         int(row0), scale, _dt(out.dtype),
-                                         _stream(q.device, stream))
+                                         int(row0), scale, _dt(out.dtype), splits, ws_ptr,
+                                         ws_bytes, _stream(q.device, stream))
     if st != DIT_OK:
         raise DitError(st, "dit_attn_stale_kv_fwd")
     return out, lse

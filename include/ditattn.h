@@ -145,6 +145,37 @@ dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const voi
                                          long long kv_head_stride, float scale, dit_stream stream);
 
 /*
+ * Split-KV form of dit_attn_chunk_fwd for problems with few queries (few
+ * (head, Q pair) work items for the persistent grid, e.g. a stale-KV patch or a
+ * short query block against long keys): every item is split over `splits`
+ * contiguous ranges of the key tiles, computed in one launch into fp32 partials
+ * in `workspace`, then merged exactly (the dit_attn_lse_merge combination) into
+ * out / lse by a second launch.  Same result as dit_attn_chunk_fwd up to fp32
+ * rounding of the merge.  The library allocates nothing: the caller passes the
+ * workspace (device memory, 256-byte aligned, at least
+ * dit_attn_splitkv_workspace_bytes(B, H, N_q, D, splits) bytes, overlapping no
+ * other argument); it is scratch, overwritten by every call, so two calls in
+ * flight at once must not share it.
+ *   arguments as dit_attn_chunk_fwd (out contiguous, of out_dtype), plus
+ *   splits : 1 (no split: workspace may be NULL) to min(64, ceil(n_kv / 128))
+ */
+dit_status dit_attn_chunk_fwd_splitkv(const void* q, const void* k, const void* v, void* out,
+                                      float* lse, int B, int H, int N_q, int n_kv, int D,
+                                      long long kv_head_stride, float scale, dit_dtype out_dtype,
+                                      int splits, void* workspace, size_t workspace_bytes,
+                                      dit_stream stream);
+
+/* Workspace bytes a split-KV call with these sizes needs (0 when splits <= 1 or a
+ * size is not positive): splits * B*H*N_q * (D + 1) * 4, the LSE part 256-byte aligned. */
+size_t dit_attn_splitkv_workspace_bytes(int B, int H, int N_q, int D, int splits);
+
+/* A split count for an N_q x n_kv problem on the current device: 1 when the
+ * persistent grid already gets at least four waves of (head, Q pair) items, else
+ * enough splits for about six waves, keeping at least 8 key tiles per split (at
+ * most 16).  Reads the device's SM count; returns 1 if it cannot. */
+int dit_attn_splitkv_suggest(int B, int H, int N_q, int n_kv);
+
+/*
  * Exact merge of p chunk partials (O_c, lse_c) of the same queries:
  *   M = max_c lse_c;  lse = M + ln sum_c exp(lse_c - M);  O = sum_c exp(lse_c - lse) O_c
  * which is what the Ring section's online-softmax accumulation over the p
@@ -166,19 +197,22 @@ dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, vo
  * hybrid SP KV buffer): a KV buffer holds K, V of all N tokens from the previous
  * diffusion step; the patch's freshly computed K, V rows [row0, row0 + m)
  * overwrite their stale rows in place, then the patch's m queries attend to the
- * whole buffer (their own rows fresh, every other row stale).  Two launches on
- * `stream`: the row update (K and V together), then the attention.
+ * whole buffer (their own rows fresh, every other row stale).  Launches on
+ * `stream`: the row update (K and V together), then the attention, split over
+ * `splits` key ranges plus a merge when splits > 1 (as dit_attn_chunk_fwd_splitkv:
+ * a patch has few queries, so splitting its long key range fills the GPU).
  *   q            : device bf16 [B, H, m, D] (the patch's queries), contiguous
  *   k_new, v_new : device bf16 [B, H, m, D], contiguous (read)
  *   k_buf, v_buf : device bf16 [B, H, N, D], contiguous (rows [row0, row0+m)
  *                  overwritten, then read)
  *   out, lse     : as dit_attn_chunk_fwd for N_q = m queries over n_kv = N keys
+ *   splits, workspace, workspace_bytes : as dit_attn_chunk_fwd_splitkv (1, NULL, 0: none)
  * 0 <= row0 <= N - m; the buffers must not overlap each other or q, k_new, v_new.
  */
 dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v_new, void* k_buf,
                                  void* v_buf, void* out, float* lse, int B, int H, int m, int N,
-                                 int D, int row0, float scale, dit_dtype out_dtype,
-                                 dit_stream stream);
+                                 int D, int row0, float scale, dit_dtype out_dtype, int splits,
+                                 void* workspace, size_t workspace_bytes, dit_stream stream);
 
 /*
  * Copies a logical [B, H, N, D] tensor of `dtype` elements from one strided

@@ -183,8 +183,9 @@ def test_layout_copy_validation(lib, kw, status):
 
 
 def stale(lib, q=Q, kn=K, vn=V, kb=ctypes.c_void_p(6 << 40), vb=ctypes.c_void_p(7 << 40), out=OUT,
-          lse=LSE, B=1, H=2, m=256, N=1024, D=128, row0=256):
-    return lib.dit_attn_stale_kv_fwd(q, kn, vn, kb, vb, out, lse, B, H, m, N, D, row0, 0.088, 0, None)
+          lse=LSE, B=1, H=2, m=256, N=1024, D=128, row0=256, splits=1, ws=None, ws_bytes=0):
+    return lib.dit_attn_stale_kv_fwd(q, kn, vn, kb, vb, out, lse, B, H, m, N, D, row0, 0.088, 0,
+                                     splits, ws, ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -195,9 +196,46 @@ def stale(lib, q=Q, kn=K, vn=V, kb=ctypes.c_void_p(6 << 40), vb=ctypes.c_void_p(
     (dict(kb=ctypes.c_void_p((7 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),   # k_buf inside v_buf
     (dict(kn=ctypes.c_void_p((6 << 40) + 1024)), da.DIT_ERR_INVALID_ARG),   # k_new inside k_buf
     (dict(out=ctypes.c_void_p((2 << 40) + 64)), da.DIT_ERR_INVALID_ARG),    # out inside k_new
+    (dict(splits=9), da.DIT_ERR_INVALID_ARG),                               # > 8 key tiles
+    (dict(splits=2), da.DIT_ERR_INVALID_ARG),                               # no workspace
 ])
 def test_stale_kv_validation(lib, kw, status):
     assert stale(lib, **kw) == status
+
+
+WS = ctypes.c_void_p(8 << 40)
+
+
+def splitkv(lib, n_kv=1000, splits=3, ws=WS, ws_bytes=None, B=1, H=2, N=256, D=128, out=OUT):
+    if ws_bytes is None:
+        ws_bytes = lib.dit_attn_splitkv_workspace_bytes(B, H, N, D, splits)
+    return lib.dit_attn_chunk_fwd_splitkv(Q, K, V, out, LSE, B, H, N, n_kv, D, N * D * 8, 0.088, 0,
+                                          splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(splits=0), da.DIT_ERR_INVALID_ARG), (dict(splits=65, n_kv=65 * 128), da.DIT_ERR_INVALID_ARG),
+    (dict(splits=9, n_kv=1000), da.DIT_ERR_INVALID_ARG),                  # 8 key tiles only
+    (dict(ws=None), da.DIT_ERR_INVALID_ARG),
+    (dict(ws=ctypes.c_void_p((8 << 40) + 128)), da.DIT_ERR_INVALID_ARG),  # not 256-byte aligned
+    (dict(ws_bytes=1000), da.DIT_ERR_INVALID_ARG),                        # too small
+    (dict(ws=ctypes.c_void_p((4 << 40) + 256)), da.DIT_ERR_INVALID_ARG),  # workspace inside out
+    (dict(D=96), da.DIT_ERR_UNSUPPORTED),
+])
+def test_splitkv_validation(lib, kw, status):
+    assert splitkv(lib, **kw) == status
+
+
+def test_splitkv_workspace_bytes(lib):
+    f = lib.dit_attn_splitkv_workspace_bytes
+    assert f(1, 2, 256, 128, 1) == 0 and f(0, 2, 256, 128, 3) == 0
+    rows = 1 * 2 * 256
+    o = 3 * rows * 128 * 4
+    assert f(1, 2, 256, 128, 3) == (o + 255) // 256 * 256 + 3 * rows * 4
+    rows = 3 * 5 * 77
+    o = 4 * rows * 64 * 4
+    assert f(3, 5, 77, 64, 4) == (o + 255) // 256 * 256 + 4 * rows * 4
+    assert lib.dit_attn_splitkv_suggest(1, 24, 3410, 27280) == 1  # no GPU here: no SM count
 
 
 def merge(lib, p=4, parts=Q, lses=K, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, pdt=0, odt=0):
