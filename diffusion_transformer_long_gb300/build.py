@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libditattn.so")
-SOURCES = ["attn_fwd.cu", "lse_merge.cu", "layout_copy.cu", "ditattn_api.cu"]
+SOURCES = ["attn_fwd.cu", "lse_merge.cu", "layout_copy.cu", "noalloc.cu", "ditattn_api.cu"]
 HEADERS = ["attn_kernel.cuh", "sm103_ptx.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

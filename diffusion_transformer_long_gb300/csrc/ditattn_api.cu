@@ -398,6 +398,29 @@ dit_status dit_attn_chunk_fwd_splitkv(const void* q, const void* k, const void* 
                         stream, false, splits, workspace);
 }
 
+dit_status dit_attn_chunk_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                              void* out, float* lse, int B, int H, int N_q,
+                                              int n_kv, int D, long long kv_head_stride,
+                                              float scale, dit_dtype out_dtype, int splits,
+                                              dit_stream stream) {
+  dit_status s = validate_attention(q, k, v, out, lse, B, H, N_q, n_kv, D, kv_head_stride, scale,
+                                    out_dtype);
+  if (s != DIT_OK) return s;
+  const long long bh = static_cast<long long>(B) * H;
+  const int tiles = (n_kv + 127) / 128;
+  if (splits < 1 || splits > 64 || splits > tiles) return DIT_ERR_INVALID_ARG;
+  if (((N_q + 255) / 256) * bh * splits > INT_MAX) return DIT_ERR_INVALID_ARG;
+  // The partials must fit the fixed scratch; nothing in it needs to start at zero (the pass
+  // writes every partial element the merge reads).
+  if (splits > 1 && splitkv_bytes(bh * N_q, D, splits) >
+                        static_cast<long long>(ditattn::kNoAllocScratchBytes))
+    return DIT_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (splits > 1 && !(scratch = ditattn::noalloc_scratch())) return DIT_ERR_CUDA;
+  return run_contiguous(q, k, v, out, lse, B, H, N_q, n_kv, D, kv_head_stride, scale, out_dtype,
+                        stream, false, splits, scratch);
+}
+
 dit_status dit_attn_lse_merge(const void* partials, const float* lses, int p, void* out,
                               float* lse, int B, int H, int N, int D, dit_dtype partial_dtype,
                               dit_dtype out_dtype, dit_stream stream) {

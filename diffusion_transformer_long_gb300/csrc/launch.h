@@ -69,6 +69,11 @@ struct CopyLaunch {
 // Row-vectorised strided copy between two views (the layout-copy kernel).
 cudaError_t launch_layout_copy(const CopyLaunch& a, cudaStream_t st);
 
+// Size of the library's fixed device scratch (noalloc.cu) and its address on the current
+// device (null on failure).
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(128) << 20;
+void* noalloc_scratch();
+
 // Test-only failure injection behind dit_test_inject_stall.
 void set_stall_injection(int enable, long long wait_limit_cycles);
 

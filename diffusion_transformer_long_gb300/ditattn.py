@@ -23,6 +23,7 @@ EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_fwd_strided", "dit_attn_chunk_fwd"
                     "dit_attn_chunk_fwd_accumulate", "dit_attn_lse_merge", "dit_layout_copy",
                     "dit_attn_stale_kv_fwd", "dit_attn_chunk_fwd_splitkv",
                     "dit_attn_splitkv_workspace_bytes", "dit_attn_splitkv_suggest",
+                    "dit_attn_chunk_fwd_splitkv_noalloc",
                     "dit_attn_check", "dit_test_inject_stall", "dit_test_set_grid_limit",
                     "dit_status_string", "dit_version")
 
@@ -65,6 +66,9 @@ def lib() -> ctypes.CDLL:
         L.dit_attn_chunk_fwd_splitkv.restype = I
         L.dit_attn_chunk_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, I, P,
                                                  ctypes.c_size_t, P]
+        L.dit_attn_chunk_fwd_splitkv_noalloc.restype = I
+        L.dit_attn_chunk_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I,
+                                                         I, P]
         L.dit_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
         L.dit_attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
         L.dit_attn_splitkv_suggest.restype = I
@@ -288,6 +292,31 @@ def attn_chunk_fwd_splitkv(q, k, v, out=None, lse=None, scale=None, out_dtype=to
                                               ws_ptr, ws_bytes, _stream(q.device, stream))
     if st != DIT_OK:
         raise DitError(st, "dit_attn_chunk_fwd_splitkv")
+    return out, lse
+
+
+def attn_chunk_fwd_splitkv_noalloc(q, k, v, out, lse, scale=None, splits=None, stream=None):
+    """Split-KV attention into the caller's out / lse with the library's fixed device scratch:
+    no allocation on this path (out and lse are required).  splits=None asks the library.
+    Calls overlapping in time race on the one scratch array."""
+    _check_qkv(q, k, v)
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v chunk must be [B, H, n_kv, D] matching q")
+    hs = kv_head_stride(k)
+    if kv_head_stride(v) != hs:
+        raise ValueError("k and v chunks must have the same head stride")
+    n_kv = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    with torch.cuda.device(q.device):
+        if splits is None:
+            splits = int(lib().dit_attn_splitkv_suggest(B, H, Nq, n_kv))
+        st = lib().dit_attn_chunk_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                                      _ptr(lse), B, H, Nq, n_kv, D, hs, scale,
+                                                      _dt(out.dtype), splits,
+                                                      _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_chunk_fwd_splitkv_noalloc")
     return out, lse
 
 

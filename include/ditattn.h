@@ -165,6 +165,23 @@ dit_status dit_attn_chunk_fwd_splitkv(const void* q, const void* k, const void* 
                                       int splits, void* workspace, size_t workspace_bytes,
                                       dit_stream stream);
 
+/*
+ * dit_attn_chunk_fwd_splitkv without a caller workspace and without any device
+ * allocation: the fp32 partials live in the library's own fixed device scratch
+ * array of 128 MiB (set up once per device).  The pages have no counterpart; this
+ * serves callers that must not allocate.  Requests whose partials need more than
+ * 128 MiB (dit_attn_splitkv_workspace_bytes > 2^27) return DIT_ERR_UNSUPPORTED;
+ * splits == 1 uses no scratch.  Nothing in the scratch needs clearing: the pass
+ * writes every partial before the merge reads it.  There is one scratch array per
+ * device: calls that overlap in time (other streams or host threads) race on it
+ * and must be serialised by the caller.
+ */
+dit_status dit_attn_chunk_fwd_splitkv_noalloc(const void* q, const void* k, const void* v,
+                                              void* out, float* lse, int B, int H, int N_q,
+                                              int n_kv, int D, long long kv_head_stride,
+                                              float scale, dit_dtype out_dtype, int splits,
+                                              dit_stream stream);
+
 /* Workspace bytes a split-KV call with these sizes needs (0 when splits <= 1 or a
  * size is not positive): splits * B*H*N_q * (D + 1) * 4, the LSE part 256-byte aligned. */
 size_t dit_attn_splitkv_workspace_bytes(int B, int H, int N_q, int D, int splits);

@@ -226,6 +226,16 @@ def test_splitkv_validation(lib, kw, status):
     assert splitkv(lib, **kw) == status
 
 
+def test_noalloc_splitkv_rejects_beyond_scratch_before_any_cuda_call(lib):
+    # Wan2.2-sized queries with 8 key splits need 2.7 GB of partials; the scratch is 128 MiB.
+    B, H, N, D = 1, 24, 27280, 128
+    st = lib.dit_attn_chunk_fwd_splitkv_noalloc(Q, K, V, OUT, LSE, B, H, N, N, D, N * D, 0.088, 0,
+                                                8, None)
+    assert st == da.DIT_ERR_UNSUPPORTED
+    assert lib.dit_attn_chunk_fwd_splitkv_noalloc(Q, K, V, OUT, LSE, B, H, N, N, D, N * D, 0.088,
+                                                  0, 0, None) == da.DIT_ERR_INVALID_ARG
+
+
 def test_splitkv_workspace_bytes(lib):
     f = lib.dit_attn_splitkv_workspace_bytes
     assert f(1, 2, 256, 128, 1) == 0 and f(0, 2, 256, 128, 3) == 0
