@@ -39,6 +39,13 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 L2_BYTES = 129e6
 
 
+def pct(xs):
+    """median, min and 90th percentile of per-step times (ms)."""
+    ys = sorted(xs)
+    return {"median": statistics.median(ys), "min": ys[0],
+            "p90": ys[min(len(ys) - 1, int(math.ceil(0.9 * len(ys))) - 1)], "n": len(ys)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -322,14 +329,53 @@ def run_gpu(args):
         barrier(dist)
     da.check(dev)
     ms_step = max_over_ranks(dist, elapsed_ms / args.steps)
-    fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fused_ev)
+    fused_all = [a.elapsed_time(b) for a, b in fused_ev]
+    chunk_all = [a.elapsed_time(b) for a, b in chunk_ev]
+    fused_ms = statistics.mean(fused_all)
     merge_ms = statistics.mean(a.elapsed_time(b) for a, b in merge_ev)
-    chunk_ms = statistics.mean(a.elapsed_time(b) for a, b in chunk_ev)
+    chunk_ms = statistics.mean(chunk_all)
     fused_ms = max_over_ranks(dist, fused_ms)
     chunk_ms = max_over_ranks(dist, chunk_ms)
     merge_ms = max_over_ranks(dist, merge_ms)
     step_flops = 2 * w.flops  # the fused pass and the chunked pass each compute the attention
     value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    # ---- small workloads (inputs below L2): warm steps and the step as one CUDA graph ----
+    warm_ms = graph_ms = None
+    graph_err = None
+    if small:
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize(dev)
+        w0, w1 = ev(), ev()
+        w0.record(stream)
+        for _ in range(args.steps):
+            step()
+        w1.record(stream)
+        torch.cuda.synchronize(dev)
+        warm_ms = max_over_ranks(dist, w0.elapsed_time(w1) / args.steps)
+        try:
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.stream(cap):
+                step()  # eager once on the capture stream
+                torch.cuda.synchronize(dev)
+                with torch.cuda.graph(graph, stream=cap):
+                    step()
+            stream.wait_stream(cap)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            g0, g1 = ev(), ev()
+            g0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            g1.record(stream)
+            torch.cuda.synchronize(dev)
+            da.check(dev)
+            graph_ms = max_over_ranks(dist, g0.elapsed_time(g1) / args.steps)
+        except Exception as e:  # reported, not fatal: the eager numbers stand
+            graph_err = f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"
 
     # ---- chunk path with bf16 partials (a stated variant; timed outside the step) ----
     parts16 = torch.empty((p, B, H, N, D), device=dev, dtype=torch.bfloat16)
@@ -522,6 +568,11 @@ def run_gpu(args):
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V shaped like Wan2.2 TI2V-5B attention)",
             "config": workload_config(w),
             "fraction_of_peak": fused_tflops / peak_sust,
+            "step_distribution_ms": {
+                "fused": pct(fused_all), "chunk_merge": pct(chunk_all)},
+            "small_workload": None if not small else {
+                "l2_flushed_ms_per_step": ms_step, "warm_ms_per_step": warm_ms,
+                "cuda_graph_ms_per_step": graph_ms, "cuda_graph_error": graph_err},
             "paths": {
                 "fused": {"ms": fused_ms, "tflops": fused_tflops},
                 "chunk_merge": {"ms": chunk_ms, "tflops": chunk_tflops,

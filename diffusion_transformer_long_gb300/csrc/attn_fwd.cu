@@ -72,8 +72,22 @@ template <int D, bool kF32, bool kAccum = false>
 cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
   constexpr int kSmem = AttnSmem<D>::kBytes;
   auto kern = attn_fwd_kernel<D, kF32, kAccum>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  // The shared-memory opt-in is set once per device and instantiation, so that later
+  // launches are only the launch itself.
+  static std::mutex mu;
+  static bool done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+      if (e != cudaSuccess) return e;
+      done[dev] = true;
+    }
+  }
   // Persistent grid: one CTA per SM (shared memory and TMEM allow no more), each
   // walking work items blockIdx.x, blockIdx.x + gridDim.x, ...
   int ctas = sm_count();
