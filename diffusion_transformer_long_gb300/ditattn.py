@@ -505,18 +505,71 @@ def ring_attention(q, k, v, chunks, scale=None, o_run=None, lse_run=None, stream
     return o_run, lse_run
 
 
+def head_groups(n_heads, groups=3):
+    """Split n_heads heads into consecutive groups for host pipelining: small first and last
+    groups (so the first compute starts, and the last copy-back ends, early) around a large
+    middle one.  Returns [(h0, h1), ...]."""
+    if n_heads < 3 or groups < 3:
+        if n_heads < 2 or groups < 2:
+            return [(0, n_heads)]
+        return [(0, n_heads // 2), (n_heads // 2, n_heads)]
+    edge = max(1, n_heads // 6)
+    return [(0, edge), (edge, n_heads - edge), (n_heads - edge, n_heads)]
+
+
+def host_pipeline(fn, inputs, outputs, groups, device=None):
+    """Runs fn over head groups with host<->device copies overlapped with compute.
+
+    inputs / outputs: host tensors (pinned for the copies to overlap) whose first dimension is
+    the flattened (batch, head) index; groups: [(h0, h1), ...] ranges of it.  For each group,
+    its input slices are copied to the device on one stream, fn(*device_input_slices) runs on
+    the current stream and returns device tensors shaped like the output slices, and those are
+    copied back on a third stream: group g+1's upload and group g-1's download overlap group g's
+    compute.  Returns outputs once every copy has landed."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    comp = torch.cuda.current_stream(dev)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    d_in = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in inputs]
+    up.wait_stream(comp)  # the device buffers were allocated on the compute stream
+    keep = []
+    for h0, h1 in groups:
+        with torch.cuda.stream(up):
+            for dt, ht in zip(d_in, inputs):
+                dt[h0:h1].copy_(ht[h0:h1], non_blocking=True)
+        comp.wait_stream(up)
+        res = fn(*(dt[h0:h1] for dt in d_in))
+        down.wait_stream(comp)
+        with torch.cuda.stream(down):
+            for ht, r in zip(outputs, res):
+                ht[h0:h1].copy_(r, non_blocking=True)
+        keep.append(res)  # device results stay alive until their copies are done
+    down.synchronize()
+    return outputs
+
+
 def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
               partial_dtype=torch.float32, device=None, accumulate=False):
-    """User-level call.  Accepts CUDA tensors, or CPU tensors (ideally pinned) that are copied to
-    the device and whose results are copied back.  chunks=None runs the fused pass; a list of
-    chunk lengths runs the p-chunk ring decomposition, merged by a separate LSE-merge pass or,
-    with accumulate=True, hop by hop inside each chunk pass (fp32 output)."""
-    on_host = not q.is_cuda
-    if on_host:
-        dev = torch.device("cuda") if device is None else torch.device(device)
-        q = q.to(dev, non_blocking=True)
-        k = k.to(dev, non_blocking=True)
-        v = v.to(dev, non_blocking=True)
+    """User-level call.  Accepts CUDA tensors, or CPU tensors (pinned for the copies to overlap)
+    that are processed in head groups through host_pipeline, results returned in pinned host
+    memory.  chunks=None runs the fused pass; a list of chunk lengths runs the p-chunk ring
+    decomposition, merged by a separate LSE-merge pass or, with accumulate=True, hop by hop
+    inside each chunk pass (fp32 output)."""
+    if not q.is_cuda:
+        # Host tensors: pipelined over head groups (uploads, compute and downloads overlap).
+        B, H, Nq, D = q.shape
+        o_dtype = torch.float32 if (accumulate and chunks is not None) else out_dtype
+        out_h = torch.empty((B * H, Nq, D), dtype=o_dtype, pin_memory=True)
+        lse_h = torch.empty((B * H, Nq), dtype=torch.float32, pin_memory=True)
+
+        def per_group(qg, kg, vg):
+            o, l = attention(qg.unsqueeze(0), kg.unsqueeze(0), vg.unsqueeze(0), scale=scale,
+                             chunks=chunks, out_dtype=out_dtype, partial_dtype=partial_dtype,
+                             accumulate=accumulate)
+            return o[0], l[0]
+
+        flat = [t.reshape(B * H, *t.shape[2:]) for t in (q, k, v)]
+        host_pipeline(per_group, flat, [out_h, lse_h], head_groups(B * H), device)
+        return out_h.view(B, H, Nq, D), lse_h.view(B, H, Nq)
     if chunks is None:
         out, lse = attn_fwd(q, k, v, scale=scale, out_dtype=out_dtype)
     elif accumulate:
@@ -526,11 +579,4 @@ def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
     else:
         out, lse = chunk_attention(q, k, v, chunks, scale=scale, out_dtype=out_dtype,
                                    partial_dtype=partial_dtype)
-    if on_host:
-        out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream(q.device).synchronize()
-        return out_h, lse_h
     return out, lse

@@ -398,3 +398,28 @@ def test_output_16_byte_aligned_not_32(dtype):
     assert torch.equal(o, o_al)
     assert (big[:shift] == 7.0).all() and (big[shift + n:] == 7.0).all()
     assert_parity(o, lse, o_ref, lse_ref, f"16B-aligned {dtype}", bf16_out=dtype == torch.bfloat16)
+
+
+# ----------------------------------------------------------------- host tensors, pipelined
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_tensors_pipelined_over_head_groups(pinned):
+    """attention() on host tensors runs head groups through host_pipeline (upload, compute and
+    download overlapped); heads are independent, so every path must equal the device call on
+    the same data bit for bit, and the fused result must match the oracle."""
+    B, H, N, D = 2, 7, 600, 128
+    q, k, v = rand_qkv(B, H, N, D, seed=91)
+    if pinned:
+        q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    assert da.head_groups(B * H) == [(0, 2), (2, 12), (12, 14)]
+    qd, kd, vd = to_dev(q, k, v)
+    chunks = [200, 150, 250]
+    for kw in (dict(), dict(chunks=chunks), dict(chunks=chunks, accumulate=True),
+               dict(out_dtype=torch.bfloat16)):
+        o_h, l_h = da.attention(q, k, v, **kw)
+        o_d, l_d = da.attention(qd, kd, vd, **kw)
+        da.check()
+        assert not o_h.is_cuda and o_h.is_pinned()
+        assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu()), kw
+    o_ref, lse_ref = oracle.attention(q, k, v, 1 / math.sqrt(D))
+    o_h, l_h = da.attention(q, k, v)
+    assert_parity(o_h, l_h, o_ref, lse_ref, "host pipelined fused")
