@@ -289,9 +289,7 @@ dit_status dit_layout_copy(const void* src, const dit_strides* src_strides, void
   if (!no_self_overlap(ds, B, H, N, D)) return DIT_ERR_INVALID_ARG;
   if (overlap(span(src, view_span(ss, B, H, N, D, es)), span(dst, view_span(ds, B, H, N, D, es))))
     return DIT_ERR_INVALID_ARG;
-  // One block per (b, h) and run of 256 / (D * es / 16) * 4 rows; the run count is a grid y.
-  const long long rows_per_block = (256 / (D * es / 16)) * 4;
-  if ((N + rows_per_block - 1) / rows_per_block > 65535) return DIT_ERR_UNSUPPORTED;
+  if (N > ditattn::layout_copy_max_rows(D, es)) return DIT_ERR_UNSUPPORTED;
   ditattn::CopyLaunch a;
   a.src = src;
   a.dst = dst;
@@ -335,7 +333,7 @@ dit_status dit_attn_stale_kv_fwd(const void* q, const void* k_new, const void* v
   s = validate_splits(splits, N, workspace, workspace_bytes, B, H, m, D,
                       {rq, rkn, rvn, rkb, rvb, ro, rl});
   if (s != DIT_OK) return s;
-  if ((m + 63) / 64 > 65535) return DIT_ERR_UNSUPPORTED;  // copy grid (bf16, D <= 128)
+  if (m > ditattn::layout_copy_max_rows(D, 2)) return DIT_ERR_UNSUPPORTED;  // copy grid
   // 1) fresh patch rows overwrite their stale rows, K and V in one launch
   ditattn::CopyLaunch c;
   c.src = k_new;

@@ -68,6 +68,8 @@ struct CopyLaunch {
 
 // Row-vectorised strided copy between two views (the layout-copy kernel).
 cudaError_t launch_layout_copy(const CopyLaunch& a, cudaStream_t st);
+// Most rows per (b, h) head one layout-copy launch handles (its grid height limit).
+long long layout_copy_max_rows(int d, int elem_bytes);
 
 // Size of the library's fixed device scratch (noalloc.cu) and its address on the current
 // device (null on failure).

@@ -176,7 +176,7 @@ def copy(lib, src=Q, ss=None, dst=OUT, ds=None, B=2, H=3, N=256, D=128, dt=1):
     (dict(ss=(1, 128, 384)), da.DIT_ERR_INVALID_ARG),
     (dict(ds=(98304, 128, 64)), da.DIT_ERR_INVALID_ARG),               # dst rows overlap
     (dict(dst=ctypes.c_void_p((1 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),  # dst inside src
-    (dict(N=70000 * 64), da.DIT_ERR_UNSUPPORTED),                      # copy grid too tall
+    (dict(N=65535 * 128 + 1), da.DIT_ERR_UNSUPPORTED),                 # copy grid too tall
 ])
 def test_layout_copy_validation(lib, kw, status):
     assert copy(lib, **kw) == status
