@@ -423,3 +423,35 @@ def test_host_tensors_pipelined_over_head_groups(pinned):
     o_ref, lse_ref = oracle.attention(q, k, v, 1 / math.sqrt(D))
     o_h, l_h = da.attention(q, k, v)
     assert_parity(o_h, l_h, o_ref, lse_ref, "host pipelined fused")
+
+
+@pytest.mark.parametrize("amp", [8.0, 30.0])
+def test_extreme_logits_every_path(amp):
+    """Q and K scaled so that scaled scores reach ~amp^2 (about 3000 for amp = 30): the
+    softmax is one-hot per row and any missing max subtraction overflows fp32.  Every path
+    must match the oracle (which subtracts the exact max in fp64).
+
+    O is held to the usual tolerances.  The LSE of such rows is about the top score, whose
+    fp32 accumulation over D products of magnitude ~1e4 (the tensor core's fp32 sum) carries
+    a few fp32 ulps of error at |lse| ~ 3000 (one ulp = 2.4e-4), so beyond the workloads'
+    range the LSE bound is 1e-3 plus 16 fp32 ulps of |lse|."""
+    B, H, N, D = 1, 2, 900, 128
+    q, k, v = rand_qkv(B, H, N, D, seed=int(amp), scale=amp)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    assert np.abs(lse_ref).max() > (500 if amp > 10 else 20)
+    qd, kd, vd = to_dev(q, k, v)
+    chunks = (300, 257, 343)
+    for name, (o, lse) in {
+        "fused": da.attn_fwd(qd, kd, vd, scale=scale),
+        "chunk+merge": da.chunk_attention(qd, kd, vd, chunks, scale=scale),
+        "ring": da.ring_attention(qd, kd, vd, chunks, scale=scale),
+        "split-kv": da.attn_chunk_fwd_splitkv(qd, kd, vd, scale=scale, splits=3),
+    }.items():
+        da.check()
+        assert torch.isfinite(o).all() and torch.isfinite(lse).all(), name
+        ulp = np.power(2.0, np.floor(np.log2(np.maximum(np.abs(lse_ref), 1e-30))) - 23)
+        lerr = np.abs(lse.double().cpu().numpy() - lse_ref)
+        assert (lerr <= 1e-3 + 16 * ulp).all(), f"amp {amp} {name}: lse {lerr.max():.3e}"
+        err = np.abs(o.double().cpu().numpy() - o_ref)
+        assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, f"amp {amp} {name}: {err.max()}"
