@@ -7,13 +7,16 @@
 // (MindIE-SD parallelism docs, "Ring Sequence Parallel" usage example: local
 // attention; arganzheng.life multi-GPU diffusion parallelism, section 4.2 Ring:
 // one KV block per round, combined by online softmax).  The same kernel serves
-// the fused pass (n_kv = N) and one KV chunk of the ring decomposition (K/V
-// pointers offset to the chunk, n_kv = chunk length, explicit head stride).
+// the fused pass (n_kv = N), one KV chunk of the ring decomposition, the ring hop
+// merged into a running (O, lse) (kAccum), and split-KV partials.  Q/K/V are read
+// through 4-D tensor maps (d, rows, heads, batch) with any strides, O is written
+// through per-head offsets and a row stride, so token-major (BSND) views work too.
 //
-// Persistent: one CTA per SM walks work items (head bh, pair of 128-row Q tiles)
-// w = blockIdx.x, blockIdx.x + gridDim.x, ...  (head-major, so the CTAs resident at
-// any moment share a head's K/V in L2).  Every barrier's phase count runs on across
-// items, so the next item's Q load and first S MMAs overlap this item's epilogue.
+// Persistent: one CTA per SM walks work items (head bh, pair of 128-row Q tiles,
+// key range) w = blockIdx.x, blockIdx.x + gridDim.x, ...  (head-major, so the CTAs
+// resident at any moment share a head's K/V in L2; the key range is the whole key
+// set unless split-KV).  Every barrier's phase count runs on across items, so the
+// next item's Q load and first S MMAs overlap this item's epilogue.
 //
 // CTA organisation (512 threads, four warpgroups):
 //   warps 0-3   softmax for Q tile 0   (thread = query row = TMEM lane)
@@ -28,7 +31,7 @@
 // Tensor memory (512 columns): S0 | S1 | O0 | O1, fp32, lane = query row.
 // Shared memory: Q0, Q1, P0, P1 (bf16 probabilities, written by the softmax
 // warps in the 128-byte-swizzled K-major layout the MMA reads), the K/V ring and
-// the per-row normalisers handed from the softmax to the epilogue.
+// the per-row scale factors handed from the softmax to the epilogue.
 //
 // Pipeline.  A softmax warpgroup releases its S buffer (S_EMPTY) as soon as
 // the scores are in registers, so the S issuer computes S_t(g+1) = Q_t K^T while
@@ -38,8 +41,8 @@
 // or overwrites the P_t buffer.  Q_EMPTY (last S MMA of an item done) lets the
 // producer refill Q; at an item's end softmax t publishes 1/rowsum (EPI_READY) and
 // moves on; the epilogue warpgroup takes it (EPI_TAKEN), waits for the last PV,
-// reads O_t and releases it (O_EMPTY) to the next item's first PV.  The K/V ring is filled in consumption order: K0, K1, V0, K2,
-// V1, ... per item.
+// reads O_t and releases it (O_EMPTY) to the next item's first PV.  The K/V ring is
+// filled in consumption order: K0, K1, V0, K2, V1, ... per item.
 //
 // Online softmax (base 2, scale folded into log2e): the running max m is only
 // raised when a tile's max exceeds it by more than kRescaleLog2 (then O and the
