@@ -57,10 +57,15 @@ def load_peaks():
 
 
 def kernel_source_digest() -> str:
+    """Digest of the attention kernel's code (comments and blank lines excluded, so that a
+    comment edit does not orphan the profile summary taken on the same code)."""
     h = hashlib.sha256()
     for f in ("attn_kernel.cuh", "sm103_ptx.cuh", "attn_fwd.cu"):
-        with open(os.path.join(ROOT, "diffusion_transformer_long_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "diffusion_transformer_long_gb300", "csrc", f)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].strip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
