@@ -378,9 +378,15 @@ def run_gpu(args):
             g1.record(stream)
             torch.cuda.synchronize(dev)
             da.check(dev)
-            graph_ms = max_over_ranks(dist, g0.elapsed_time(g1) / args.steps)
+            graph_ms = g0.elapsed_time(g1) / args.steps
         except Exception as e:  # reported, not fatal: the eager numbers stand
             graph_err = f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"
+        # collectives outside the try: every rank takes part whatever happened locally
+        all_ok = sum_over_ranks(dist, 1.0 if graph_ms is not None else 0.0) == world
+        slowest = max_over_ranks(dist, graph_ms if graph_ms is not None else 0.0)
+        graph_ms = slowest if all_ok else None
+        if not all_ok and graph_err is None:
+            graph_err = "CUDA-graph capture failed on another rank"
 
     # ---- chunk path with bf16 partials (a stated variant; timed outside the step) ----
     parts16 = torch.empty((p, B, H, N, D), device=dev, dtype=torch.bfloat16)
