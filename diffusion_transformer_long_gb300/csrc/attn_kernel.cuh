@@ -38,7 +38,9 @@
 // softmax t is still turning S_t(g) into probabilities; softmax t starts the next
 // tile the moment it has published P_t(g) (P_FULL).  O_t += P_t V is committed to
 // its own barrier (PV_DONE), which softmax t waits on only before it rescales O_t
-// or overwrites the P_t buffer.  Q_EMPTY (last S MMA of an item done) lets the
+// or overwrites the P_t buffer.  P_t is published in two halves (keys 0-63 on P_LO,
+// 64-127 on P_FULL), so the PV issuer starts on the first half while the softmax still
+// computes the second.  Q_EMPTY (last S MMA of an item done) lets the
 // producer refill Q; at an item's end softmax t publishes 1/rowsum (EPI_READY) and
 // moves on; the epilogue warpgroup takes it (EPI_TAKEN), waits for the last PV,
 // reads O_t and releases it (O_EMPTY) to the next item's first PV.  The K/V ring is
@@ -150,7 +152,8 @@ struct AttnSmem {
   static constexpr int bKVEmpty = bVFull + kStages;  // + slot: the slot's tile was consumed
   static constexpr int bSFull = bKVEmpty + kStages;  // + tile: S_t computed (MMA commit)
   static constexpr int bSEmpty = bSFull + 2;         // + tile: S_t read into registers (128 arrivals)
-  static constexpr int bPFull = bSEmpty + 2;         // + tile: P_t written (128 arrivals)
+  static constexpr int bPLo = bSEmpty + 2;           // + tile: keys 0-63 of P_t written (128)
+  static constexpr int bPFull = bPLo + 2;            // + tile: keys 64-127 of P_t written (128)
   static constexpr int bPVDone = bPFull + 2;         // + tile: O_t += P_t V done (MMA commit)
   static constexpr int bOEmpty = bPVDone + 2;        // + tile: O_t read by the epilogue (128 arrivals)
   static constexpr int bEpiReady = bOEmpty + 2;      // + tile: normaliser of an item written (128)
@@ -168,10 +171,11 @@ struct AttnSmem {
 
 namespace detail {
 
-// Bounded wait that also gives up when another role has aborted.
+// Bounded wait that also gives up when another role has aborted.  A phase that has already
+// completed is seen by the non-blocking test first; otherwise try_wait suspends the thread.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               const volatile int* abort_flag, long long limit) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!ptx::mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
@@ -406,11 +410,11 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
   constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, D, false, true);
   const Descs<D> ds(sbase);
   // P K-major, V MN-major (D contiguous); 16 keys (2 KB of V) per instruction.
-  auto issue = [&](int t, int slot, bool acc) {
+  auto issue = [&](int t, int slot, bool acc, int half) {
     const uint32_t vb = Descs<D>::pick(ds.v, slot);
     const uint32_t pa = ds.pp[t];
 #pragma unroll
-    for (int k = 0; k < kBlockN / 16; ++k) {
+    for (int k = half * 4; k < half * 4 + 4; ++k) {
       const uint32_t aoff = ((k / 4) * L::kRegion + (k % 4) * 32) >> 4;
       ptx::mma_bf16_ss(tmem + 2 * kBlockN + t * D, Descs<D>::full(pa + aoff),
                        Descs<D>::full(vb + k * 128), kIdesc, (acc || k > 0) ? 1u : 0u);
@@ -429,7 +433,7 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
     const int n_tiles = item_of(p, w).ntiles;
     for (int j = 0; j < n_tiles; ++j, ++g) {
       const int sV = (ring0 + v_item(j, n_tiles)) % kStages;
-      if (!(ok = wait(L::bPFull + 0, g & 1))) break;
+      if (!(ok = wait(L::bPLo + 0, g & 1))) break;
       DIT_TRACE(kTrMmaP0, g);
       ok = wait(L::bVFull + sV, (vpar >> sV) & 1);
       vpar ^= 1u << sV;
@@ -438,14 +442,20 @@ __device__ __forceinline__ void pv_issuer(const AttnParams& p, uint32_t sbase, u
       // The first PV of an item overwrites O_t: the previous item's epilogue must have read it.
       if (j == 0 && li > 0 && !(ok = wait(L::bOEmpty + 0, (li - 1) & 1))) break;
       ptx::tc_fence_after();
-      issue(0, sV, j > 0);
+      issue(0, sV, j > 0, 0);
+      if (!(ok = wait(L::bPFull + 0, g & 1))) break;
+      ptx::tc_fence_after();
+      issue(0, sV, j > 0, 1);
       ptx::mma_commit(bar(L::bPVDone + 0));
       DIT_TRACE(kTrMmaPv0, g);
-      if (!(ok = wait(L::bPFull + 1, g & 1))) break;
+      if (!(ok = wait(L::bPLo + 1, g & 1))) break;
       DIT_TRACE(kTrMmaP1, g);
       if (j == 0 && li > 0 && !(ok = wait(L::bOEmpty + 1, (li - 1) & 1))) break;
       ptx::tc_fence_after();
-      issue(1, sV, j > 0);
+      issue(1, sV, j > 0, 0);
+      if (!(ok = wait(L::bPFull + 1, g & 1))) break;
+      ptx::tc_fence_after();
+      issue(1, sV, j > 0, 1);
       ptx::mma_commit(bar(L::bPVDone + 1));
       ptx::mma_commit(bar(L::bKVEmpty + sV));
       DIT_TRACE(kTrMmaPv1, g);
@@ -575,23 +585,11 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
         ptx::tmem_wait_st();
       }
 
-      // P = 2^(c*s - m), two elements per packed FMA.
+      // P = 2^(c*s - m), two elements per packed FMA, written in two halves (keys 0-63,
+      // 64-127: one 128-byte-swizzled K-major region each) so that the PV GEMM can start
+      // on the first while the second is computed.
       const uint64_t c2 = ptx::f2pack(c, c);
       const uint64_t nm2 = ptx::f2pack(-m, -m);
-#pragma unroll
-      for (int i = 0; i < kBlockN; i += 2) {
-        float x0, x1;
-        ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[i], s[i + 1]), c2, nm2), x0, x1);
-        s[i] = ptx::ex2_approx(x0);
-        s[i + 1] = ptx::ex2_approx(x1);
-      }
-      if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, g);
-
-      // The P_t buffer is free once PV_t(g-1) has read it.
-      if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
-
-      // Pack P to bf16, store it (row r -> two 128-byte-swizzled K-major regions: keys
-      // 0-63, 64-127), and accumulate both row sums in independent chains.
       uint64_t acc_l[4];
       float acc_lp[8];
 #pragma unroll
@@ -599,24 +597,40 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc_lp[q] = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < kBlockN / 8; ++ch) {
-        uint32_t wv[4];
+      for (int half = 0; half < 2; ++half) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float p0 = s[8 * ch + 2 * q], p1 = s[8 * ch + 2 * q + 1];
-          wv[q] = ptx::pack_bf16x2(p0, p1);
-          acc_l[q] = ptx::fadd2(acc_l[q], ptx::f2pack(p0, p1));
-          add_bf16x2(acc_lp[2 * q], acc_lp[2 * q + 1], wv[q]);
+        for (int i = half * 64; i < half * 64 + 64; i += 2) {
+          float x0, x1;
+          ptx::f2unpack(ptx::ffma2(ptx::f2pack(s[i], s[i + 1]), c2, nm2), x0, x1);
+          s[i] = ptx::ex2_approx(x0);
+          s[i + 1] = ptx::ex2_approx(x1);
         }
-        const uint32_t addr = sP + (ch / 8) * L::kRegion + r * 128 +
-                              ((static_cast<uint32_t>(ch % 8) ^ sw) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]),
-                     "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                     : "memory");
+        if (half == 0) {
+          if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, g);
+          // The P_t buffer is free once PV_t(g-1) has read it.
+          if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+        }
+#pragma unroll
+        for (int ch = half * 8; ch < half * 8 + 8; ++ch) {
+          uint32_t wv[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float p0 = s[8 * ch + 2 * q], p1 = s[8 * ch + 2 * q + 1];
+            wv[q] = ptx::pack_bf16x2(p0, p1);
+            acc_l[q] = ptx::fadd2(acc_l[q], ptx::f2pack(p0, p1));
+            add_bf16x2(acc_lp[2 * q], acc_lp[2 * q + 1], wv[q]);
+          }
+          const uint32_t addr = sP + half * L::kRegion + r * 128 +
+                                ((static_cast<uint32_t>(ch % 8) ^ sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]),
+                       "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                       : "memory");
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(half == 0 ? L::bPLo + t : L::bPFull + t));
       }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(L::bPFull + t));
+      if (!ok) break;
       if (r == 0) DIT_TRACE(kTrSmArrive0 + 5 * t, g);
       {
         const uint64_t sl =
@@ -903,6 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(L::bSFull + t), 1);
       ptx::mbar_init(bar(L::bSEmpty + t), kBlockM);
       ptx::mbar_init(bar(L::bPFull + t), kBlockM);
+      ptx::mbar_init(bar(L::bPLo + t), kBlockM);
       ptx::mbar_init(bar(L::bPVDone + t), 1);
       ptx::mbar_init(bar(L::bOEmpty + t), kBlockM);
       ptx::mbar_init(bar(L::bEpiReady + t), kBlockM);
