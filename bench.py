@@ -189,11 +189,13 @@ def sum_over_ranks(dist, x: float) -> float:
     return float(t.item())
 
 
-def oracle_sample_tflops(w, q, k, v, target_s: float, rows_cap: int = 100000):
-    """Times the fp64 oracle on a bounded row sample of workload w (all heads, R query rows).
+def oracle_sample_tflops(w, q, k, v, target_s: float, rows_cap: int = 100000,
+                         threads: int = 0):
+    """Times the fp64 oracle on a bounded row sample of workload w (all heads, R query rows),
+    on `threads` worker threads (0: every core this process may run on).
     Returns (tflops, seconds, rows_per_head, threads)."""
     import oracle
-    threads = len(os.sched_getaffinity(0))
+    threads = threads or len(os.sched_getaffinity(0))
     heads = w.B * w.H
     # calibrate on 2 rows per head
     t0 = time.perf_counter()
@@ -581,6 +583,12 @@ def run_gpu(args):
             cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
                    "sample": f"{B * H} heads x {rows} query rows against all {N} keys "
                              f"({secs:.1f} s of fp64 oracle)"}
+            # The same oracle on one core, over a smaller sample.
+            tf1, secs1, rows1, _ = oracle_sample_tflops(
+                w, q_h, k_h, v_h, target_s=min(4.0, args.cpu_baseline_s / 3), threads=1)
+            cpu["single_core"] = {"value": tf1, "cores": 1,
+                                  "sample": f"{B * H} heads x {rows1} query rows "
+                                            f"({secs1:.1f} s)"}
         clocks = clk.summary()
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
