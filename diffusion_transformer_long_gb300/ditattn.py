@@ -517,6 +517,17 @@ def head_groups(n_heads, groups=3):
     return [(0, edge), (edge, n_heads - edge), (n_heads - edge, n_heads)]
 
 
+_PIPE_STREAMS = {}
+
+
+def _pipeline_streams(dev: torch.device):
+    """Upload and download streams of host_pipeline, created once per device."""
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    if key not in _PIPE_STREAMS:
+        _PIPE_STREAMS[key] = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
+    return _PIPE_STREAMS[key]
+
+
 def host_pipeline(fn, inputs, outputs, groups, device=None):
     """Runs fn over head groups with host<->device copies overlapped with compute.
 
@@ -525,10 +536,12 @@ def host_pipeline(fn, inputs, outputs, groups, device=None):
     its input slices are copied to the device on one stream, fn(*device_input_slices) runs on
     the current stream and returns device tensors shaped like the output slices, and those are
     copied back on a third stream: group g+1's upload and group g-1's download overlap group g's
-    compute.  Returns outputs once every copy has landed."""
+    compute.  Returns outputs once every copy has landed.  (Alternating the groups over two
+    compute streams, so that one group's kernels fill the previous group's last wave, measured
+    slower.)"""
     dev = torch.device("cuda") if device is None else torch.device(device)
     comp = torch.cuda.current_stream(dev)
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    up, down = _pipeline_streams(dev)
     d_in = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in inputs]
     up.wait_stream(comp)  # the device buffers were allocated on the compute stream
     keep = []
