@@ -2,8 +2,10 @@
 
 One step = the whole hot path once over one batch of synthetic input: the
 fused attention pass (dit_attn_fwd) and the same attention as p KV chunks
-(p x dit_attn_chunk_fwd, one per virtual ring rank) merged by
-dit_attn_lse_merge.  FLOPs counted per pass: 4*B*H*N^2*D (the two GEMMs).
+(dit_attn_chunks_fwd: every virtual ring rank's local attention, partial O and
+LSE per chunk, in one launch) merged by dit_attn_lse_merge.  The same chunk path
+with one dit_attn_chunk_fwd launch per rank (bitwise the same partials) is
+reported beside the step.  FLOPs counted per pass: 4*B*H*N^2*D (the two GEMMs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload wan22] [--impl reference]
 
@@ -290,9 +292,7 @@ def run_gpu(args):
             fused_ev.append((e0, e1))
             c0 = ev()
             c0.record(stream)
-        for c, (s, n) in enumerate(zip(starts, w.chunks)):
-            da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=parts[c], lse=lses[c],
-                              scale=w.scale)
+        da.attn_chunks_fwd(q, k, v, w.chunks, partials=parts, lses=lses, scale=w.scale)
         if record:
             m0, m1 = ev(), ev()
             m0.record(stream)
@@ -302,7 +302,7 @@ def run_gpu(args):
             merge_ev.append((m0, m1))
             chunk_ev.append((c0, m1))
 
-    launches_per_step = 1 + p + 1
+    launches_per_step = 3
     for _ in range(args.warmup):
         step()
         if flush is not None:
@@ -390,27 +390,37 @@ def run_gpu(args):
         if not all_ok and graph_err is None:
             graph_err = "CUDA-graph capture failed on another rank"
 
-    # ---- chunk path with bf16 partials (a stated variant; timed outside the step) ----
+    # ---- chunk-path variants (timed outside the step) ----
     parts16 = torch.empty((p, B, H, N, D), device=dev, dtype=torch.bfloat16)
 
     def chunk_bf16():
-        for c, (s, n) in enumerate(zip(starts, w.chunks)):
-            da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=parts16[c], lse=lses[c],
-                              scale=w.scale)
+        # bf16 partials (a stated variant), all ranks in one launch
+        da.attn_chunks_fwd(q, k, v, w.chunks, partials=parts16, lses=lses, scale=w.scale)
         da.attn_lse_merge(parts16, lses, out=out_c, lse=lse_c)
 
-    for _ in range(args.warmup):
-        chunk_bf16()
-    torch.cuda.synchronize(dev)
-    b0, b1 = ev(), ev()
-    b0.record(stream)
-    n16 = max(3, args.steps // 3)
-    for _ in range(n16):
-        chunk_bf16()
-    b1.record(stream)
-    torch.cuda.synchronize(dev)
-    da.check(dev)
-    chunk16_ms = max_over_ranks(dist, b0.elapsed_time(b1) / n16)
+    def chunk_per_rank():
+        # one dit_attn_chunk_fwd launch per virtual rank (the same partials, bit for bit)
+        for c, (s, n) in enumerate(zip(starts, w.chunks)):
+            da.attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=parts[c], lse=lses[c],
+                              scale=w.scale)
+        da.attn_lse_merge(parts, lses, out=out_c, lse=lse_c)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        b0, b1 = ev(), ev()
+        b0.record(stream)
+        n_rep = max(3, args.steps // 3)
+        for _ in range(n_rep):
+            fn()
+        b1.record(stream)
+        torch.cuda.synchronize(dev)
+        da.check(dev)
+        return max_over_ranks(dist, b0.elapsed_time(b1) / n_rep)
+
+    chunk16_ms = timed(chunk_bf16)
+    per_rank_ms = timed(chunk_per_rank)
     del parts16
 
     # ---- hop-by-hop ring: each chunk pass merges into the running (O, lse) itself ----
@@ -536,7 +546,7 @@ def run_gpu(args):
     def both_paths(qg, kg, vg):
         q4, k4, v4 = qg.unsqueeze(0), kg.unsqueeze(0), vg.unsqueeze(0)
         o1, l1 = da.attn_fwd(q4, k4, v4, scale=w.scale)
-        o2, l2 = da.chunk_attention(q4, k4, v4, w.chunks, scale=w.scale)
+        o2, l2 = da.chunk_attention(q4, k4, v4, w.chunks, scale=w.scale, batched=True)
         return o1[0], l1[0], o2[0], l2[0]
 
     def e2e_step():
@@ -611,6 +621,9 @@ def run_gpu(args):
                 "chunk_merge_bf16_partials": {"ms": chunk16_ms,
                                               **tf_frac(w.flops / (chunk16_ms * 1e-3) / 1e12),
                                               "ratio_to_fused": chunk16_ms / fused_ms},
+                "chunk_merge_per_rank_launches": {
+                    "ms": per_rank_ms, **tf_frac(w.flops / (per_rank_ms * 1e-3) / 1e12),
+                    "ratio_to_fused": per_rank_ms / fused_ms, "launches": p + 1},
                 "ring_accumulate": {"ms": ring_ms,
                                     **tf_frac(w.flops / (ring_ms * 1e-3) / 1e12),
                                     "ratio_to_fused": ring_ms / fused_ms,
@@ -666,6 +679,9 @@ def run_profile_case(args):
     if args.profile_case == "merge":
         parts = torch.randn((p, B, H, N, D), device=dev)
         lses = torch.randn((p, B, H, N), device=dev)
+    if args.profile_case == "chunks":
+        parts = torch.empty((p, B, H, N, D), device=dev)
+        lses = torch.empty((p, B, H, N), device=dev)
     if args.profile_case == "transpose":
         src = da.bhnd_to_bsnd(q)
         dst = torch.empty_like(q)
@@ -673,6 +689,8 @@ def run_profile_case(args):
     for _ in range(args.warmup + args.steps):
         if args.profile_case == "fused":
             da.attn_fwd(q, k, v, out=out, lse=lse, scale=w.scale)
+        elif args.profile_case == "chunks":
+            da.attn_chunks_fwd(q, k, v, w.chunks, partials=parts, lses=lses, scale=w.scale)
         elif args.profile_case == "chunk":
             da.attn_chunk_fwd(q, k[:, :, s0:s0 + n0], v[:, :, s0:s0 + n0], out=out, lse=lse,
                               scale=w.scale)
@@ -698,7 +716,8 @@ def main(argv=None):
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
     ap.add_argument("--ref-step-s", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["fused", "chunk", "accumulate", "merge", "transpose"],
+    ap.add_argument("--profile-case", choices=["fused", "chunks", "chunk", "accumulate", "merge",
+                                               "transpose"],
                     help="run only this path, untimed (for ncu captures); prints nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -107,7 +107,10 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
       !encode_view(&prm.tm_v, a.v, a.d, a.n_kv, a.heads, a.batch, a.vs))
     return cudaErrorInvalidValue;
   const bool split = a.splits > 1;
-  if (split && (a.accumulate || !a.ws_o || !a.ws_lse)) return cudaErrorInvalidValue;
+  const bool batched = a.chunks > 0;
+  if (split && (a.accumulate || batched || !a.ws_o || !a.ws_lse)) return cudaErrorInvalidValue;
+  if (batched && (a.accumulate || a.chunks > kMaxRanges || !a.chunk_starts))
+    return cudaErrorInvalidValue;
   // Split-KV passes write fp32 partials, contiguous, into the workspace.
   const bool f32 = split || a.out_f32;
   void* const obase = split ? static_cast<void*>(a.ws_o) : a.out;
@@ -132,11 +135,14 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   prm.bh_count = a.batch * a.heads;
   prm.heads = a.heads;
   prm.q_pairs = (a.n_q + 2 * kBlockM - 1) / (2 * kBlockM);
-  prm.splits = split ? a.splits : 1;
+  prm.splits = split ? a.splits : batched ? a.chunks : 1;
   prm.tiles_total = (a.n_kv + kBlockN - 1) / kBlockN;
   const long long rows = static_cast<long long>(prm.bh_count) * a.n_q;
-  prm.ws_o_stride = split ? rows * a.d : 0;
-  prm.ws_l_stride = split ? rows : 0;
+  prm.ws_o_stride = (split || batched) ? rows * a.d : 0;
+  prm.ws_l_stride = (split || batched) ? rows : 0;
+  prm.explicit_ranges = batched ? 1 : 0;
+  for (int c = 0; c <= kMaxRanges; ++c)
+    prm.kv_starts[c] = (batched && c <= a.chunks) ? a.chunk_starts[c] : 0;
   prm.num_items = prm.q_pairs * prm.bh_count * prm.splits;
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;

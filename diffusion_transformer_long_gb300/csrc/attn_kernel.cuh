@@ -106,6 +106,7 @@ constexpr uint32_t kRegsEpilogue = 88;
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
+constexpr int kMaxRanges = 64;            // key ranges (splits or explicit chunks) per launch
 
 struct AttnParams {
   CUtensorMap tm_q;   // (D, n_q, bh) bf16, box (64, 128, 1), 128B swizzle
@@ -122,10 +123,13 @@ struct AttnParams {
   int bh_count;
   int heads;          // H: head bh is (b, h) = (bh / H, bh % H)
   int q_pairs;        // ceil(n_q / 256)
-  int splits;         // key ranges per (head, Q pair): 1, or S for split-KV partials
+  int splits;         // key ranges per (head, Q pair): 1, or S for split-KV / chunk partials
   int tiles_total;    // ceil(n_kv / 128)
-  long long ws_o_stride;  // split-KV: elements between consecutive splits' partial O (else 0)
-  long long ws_l_stride;  // split-KV: elements between consecutive splits' partial LSEs (else 0)
+  long long ws_o_stride;  // elements between consecutive ranges' partial O (0 for one range)
+  long long ws_l_stride;  // elements between consecutive ranges' partial LSEs (0 for one range)
+  int explicit_ranges;    // 1: range s is keys [kv_starts[s], kv_starts[s+1]); 0: equal tile
+                          // splits [s*T/S, (s+1)*T/S) of the T tiles
+  int kv_starts[kMaxRanges + 1];
   int num_items;      // bh_count * q_pairs * splits
   float scale_log2;   // scale * log2(e)
   long long wait_limit;  // SM clocks a bounded wait may spin before giving up
@@ -193,9 +197,10 @@ struct Item {
   int bh;      // b * H + h
   int b, h;
   int q_row0;  // first query row of the pair of Q tiles
-  int split;   // key range of the item (0 unless split-KV)
-  int tile0;   // first KV tile of the range
-  int ntiles;  // KV tiles in the range (>= 1)
+  int split;   // key range of the item (0 unless split-KV or batched chunks)
+  int kv0;     // first key row of the range
+  int kv_len;  // keys in the range (>= 1)
+  int ntiles;  // KV tiles in the range: ceil(kv_len / 128)
   __device__ __forceinline__ size_t out_off(const AttnParams& p) const {
     return static_cast<size_t>(b) * p.o_sb + static_cast<size_t>(h) * p.o_sh +
            static_cast<size_t>(split) * p.ws_o_stride;
@@ -204,16 +209,26 @@ struct Item {
     return static_cast<size_t>(bh) * p.n_q + static_cast<size_t>(split) * p.ws_l_stride;
   }
 };
-// Work item w: (head, Q pair, key range), key range fastest.  Split s of S covers KV tiles
-// [s*T/S, (s+1)*T/S) of the T tiles.
+// Work item w: (head, Q pair, key range), key range fastest.  Range s is either the tile
+// split [s*T/S, (s+1)*T/S) of the T tiles (ending at n_kv), or keys [kv_starts[s],
+// kv_starts[s+1]) (one virtual rank's chunk of the ring decomposition).
 __device__ __forceinline__ Item item_of(const AttnParams& p, int w) {
   const int qi = w / p.splits;
   const int split = w - qi * p.splits;
   const int bh = qi / p.q_pairs;
   const int b = bh / p.heads;
-  const int tile0 = static_cast<int>(static_cast<long long>(split) * p.tiles_total / p.splits);
-  const int tile1 = static_cast<int>(static_cast<long long>(split + 1) * p.tiles_total / p.splits);
-  return {bh, b, bh - b * p.heads, (qi % p.q_pairs) * 2 * kBlockM, split, tile0, tile1 - tile0};
+  int kv0, kv1;
+  if (p.explicit_ranges) {
+    kv0 = p.kv_starts[split];
+    kv1 = p.kv_starts[split + 1];
+  } else {
+    kv0 = static_cast<int>(static_cast<long long>(split) * p.tiles_total / p.splits) * kBlockN;
+    kv1 = min(p.n_kv,
+              static_cast<int>(static_cast<long long>(split + 1) * p.tiles_total / p.splits) *
+                  kBlockN);
+  }
+  return {bh, b, bh - b * p.heads, (qi % p.q_pairs) * 2 * kBlockM, split, kv0, kv1 - kv0,
+          (kv1 - kv0 + kBlockN - 1) / kBlockN};
 }
 
 // K/V ring items of one work item, in consumption order: K_0, then per KV tile j:
@@ -247,7 +262,7 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase,
   int q_loads = 0;  // Q loads issued (QFULL phases armed)
   int it = 0;       // ring index
   bool ok = true;
-  auto load = [&](bool is_v, int tile, const Item& item) {
+  auto load = [&](bool is_v, int row, const Item& item) {
     const int s = it % kStages;
     const uint32_t ph = (it / kStages) & 1;
     if (!wait(L::bKVEmpty + s, ph ^ 1)) return false;
@@ -260,7 +275,7 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase,
 #pragma unroll
     for (int r = 0; r < kRegions; ++r)
       ptx::tma_load_4d(sbase + L::kKV + s * L::kTile + r * L::kRegion, tm, bar(fb), r * 64,
-                       tile * kBlockN, item.h, item.b);
+                       row, item.h, item.b);
     DIT_TRACE(kTrProdIssue, it);
 #pragma unroll
     for (int q = 0; q < kStages; ++q)
@@ -287,10 +302,10 @@ __device__ __forceinline__ void producer(const AttnParams& p, uint32_t sbase,
     ++q_loads;
     if (p.stall_kv) return;  // test-only: the consumers' first K wait will expire
 
-    if (!(ok = load(false, item.tile0, item))) break;
+    if (!(ok = load(false, item.kv0, item))) break;
     for (int j = 0; ok && j < item.ntiles; ++j) {
-      if (j + 1 < item.ntiles && !(ok = load(false, item.tile0 + j + 1, item))) break;
-      ok = load(true, item.tile0 + j, item);
+      if (j + 1 < item.ntiles && !(ok = load(false, item.kv0 + (j + 1) * kBlockN, item))) break;
+      ok = load(true, item.kv0 + j * kBlockN, item);
     }
   }
   if (!ok) {
@@ -506,11 +521,11 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
   for (int w = blockIdx.x; ok && w < p.num_items; w += gridDim.x, ++li) {
     // Only the key range is live across the tile loop; the rest of the item is
     // recomputed at its end.
-    int ntiles, kv_left;  // tiles of the item, keys from its first tile to n_kv
+    int ntiles, kv_left;  // tiles of the item, keys in its range
     {
       const Item it = item_of(p, w);
       ntiles = it.ntiles;
-      kv_left = p.n_kv - it.tile0 * kBlockN;
+      kv_left = it.kv_len;
     }
     float m = -INFINITY;  // running max of scale*log2e*s (possibly stale by < 2^8)
     float l = 0.f;        // running sum of 2^(c*s - m), for the LSE
@@ -541,8 +556,9 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       float mx = ptx::fmax3(cmax[0], cmax[1], fmaxf(cmax[2], cmax[3]));
       const int valid = kv_left - j * kBlockN;
       if (valid < kBlockN) {
-        // Ragged last tile: keys past n_kv (zero-filled K rows) are masked to -inf and
-        // the max is taken over the valid columns only.
+        // Ragged last tile: keys past the item's range (zero-filled rows past n_kv, or the
+        // next range's rows) are masked to -inf, so their P is exactly 0, and the max is
+        // taken over the valid columns only.
 #pragma unroll
         for (int i = 0; i < kBlockN; ++i)
           if (i >= valid) s[i] = -INFINITY;

@@ -133,7 +133,8 @@ dit_status run_attention(const void* q, const dit_strides& qs, const void* k, co
                          const void* v, const dit_strides& vs, void* out, const dit_strides& os,
                          float* lse, int B, int H, int N_q, int n_kv, int D, float scale,
                          dit_dtype out_dtype, dit_stream stream, bool accumulate = false,
-                         int splits = 1, void* workspace = nullptr) {
+                         int splits = 1, void* workspace = nullptr, int chunks = 0,
+                         const int* chunk_starts = nullptr) {
   int* status = status_ptr();
   if (!status) return DIT_ERR_CUDA;
   ditattn::AttnLaunch a;
@@ -156,6 +157,8 @@ dit_status run_attention(const void* q, const dit_strides& qs, const void* k, co
   a.out_f32 = out_dtype == DIT_F32;
   a.accumulate = accumulate;
   a.splits = splits;
+  a.chunks = chunks;
+  a.chunk_starts = chunk_starts;
   if (splits > 1) {
     const long long rows = static_cast<long long>(B) * H * N_q;
     a.ws_o = static_cast<float*>(workspace);
@@ -170,11 +173,12 @@ dit_status run_attention(const void* q, const dit_strides& qs, const void* k, co
 dit_status run_contiguous(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                           int H, int N_q, int n_kv, int D, long long kv_head_stride, float scale,
                           dit_dtype out_dtype, dit_stream stream, bool accumulate = false,
-                          int splits = 1, void* workspace = nullptr) {
+                          int splits = 1, void* workspace = nullptr, int chunks = 0,
+                          const int* chunk_starts = nullptr) {
   const dit_strides qs = contiguous(H, N_q, D);
   const dit_strides kvs = {H * kv_head_stride, kv_head_stride, D};
   return run_attention(q, qs, k, kvs, v, kvs, out, qs, lse, B, H, N_q, n_kv, D, scale, out_dtype,
-                       stream, accumulate, splits, workspace);
+                       stream, accumulate, splits, workspace, chunks, chunk_starts);
 }
 
 // Split-KV arguments: 1 <= splits <= min(64, KV tiles); with splits > 1 a 256-byte-aligned
@@ -215,6 +219,30 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
   if (s != DIT_OK) return s;
   return run_contiguous(q, k, v, out_partial, lse_partial, B, H, N_q, n_kv, D, kv_head_stride,
                         scale, partial_dtype, stream);
+}
+
+dit_status dit_attn_chunks_fwd(const void* q, const void* k, const void* v, void* partials,
+                               float* lses, int B, int H, int N_q, int n_kv, int D,
+                               long long kv_head_stride, int p, const int* chunk_starts,
+                               float scale, dit_dtype partial_dtype, dit_stream stream) {
+  dit_status s = validate_attention(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride,
+                                    scale, partial_dtype);
+  if (s != DIT_OK) return s;
+  if (p < 1 || p > 64 || !chunk_starts) return DIT_ERR_INVALID_ARG;
+  if (chunk_starts[0] < 0 || chunk_starts[p] > n_kv) return DIT_ERR_INVALID_ARG;
+  for (int c = 0; c < p; ++c)
+    if (chunk_starts[c + 1] <= chunk_starts[c]) return DIT_ERR_INVALID_ARG;
+  // All p partial blocks and LSE rows must stay clear of the inputs and of each other.
+  const long long bh = static_cast<long long>(B) * H;
+  const long long rows = bh * N_q;
+  const Range rp = span(partials, p * rows * D * dtype_bytes(partial_dtype));
+  const Range rl = span(lses, p * rows * 4);
+  const long long kv_bytes = ((bh - 1) * kv_head_stride + static_cast<long long>(n_kv) * D) * 2;
+  for (Range in : {span(q, rows * D * 2), span(k, kv_bytes), span(v, kv_bytes)})
+    if (overlap(rp, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
+  if (overlap(rp, rl)) return DIT_ERR_INVALID_ARG;
+  return run_contiguous(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride, scale,
+                        partial_dtype, stream, false, 1, nullptr, p, chunk_starts);
 }
 
 dit_status dit_attn_chunk_fwd_accumulate(const void* q, const void* k, const void* v, float* o_run,

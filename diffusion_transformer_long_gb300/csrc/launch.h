@@ -36,6 +36,12 @@ struct AttnLaunch {
   int splits = 1;
   float* ws_o = nullptr;
   float* ws_lse = nullptr;
+  // Batched chunks (virtual ranks): chunk_starts (host, chunks + 1 increasing row offsets
+  // into k/v) defines `chunks` key ranges; one launch writes each chunk's partial O to
+  // out + c * B*H*N_q*D (contiguous BHND, fp32 or bf16) and its LSE to lse + c * B*H*N_q.
+  // No merge.  0 = off.
+  int chunks = 0;
+  const int* chunk_starts = nullptr;
 };
 
 // Encodes the TMA descriptors and launches the attention kernel on `st`.

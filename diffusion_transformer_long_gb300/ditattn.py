@@ -19,7 +19,7 @@ from . import build as _build
 DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = range(5)
 DIT_F32, DIT_BF16 = 0, 1
 
-EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_fwd_strided", "dit_attn_chunk_fwd",
+EXPORTED_SYMBOLS = ("dit_attn_fwd", "dit_attn_fwd_strided", "dit_attn_chunk_fwd", "dit_attn_chunks_fwd",
                     "dit_attn_chunk_fwd_accumulate", "dit_attn_lse_merge", "dit_layout_copy",
                     "dit_attn_stale_kv_fwd", "dit_attn_chunk_fwd_splitkv",
                     "dit_attn_splitkv_workspace_bytes", "dit_attn_splitkv_suggest",
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
         L.dit_layout_copy.argtypes = [P, SP, P, SP, I, I, I, I, I, P]
         L.dit_attn_chunk_fwd.restype = I
         L.dit_attn_chunk_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, I, P]
+        L.dit_attn_chunks_fwd.restype = I
+        L.dit_attn_chunks_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, I, ctypes.POINTER(I), F,
+                                          I, P]
         L.dit_attn_chunk_fwd_accumulate.restype = I
         L.dit_attn_chunk_fwd_accumulate.argtypes = [P, P, P, P, P, I, I, I, I, I, LL, F, P]
         L.dit_attn_lse_merge.restype = I
@@ -396,6 +399,43 @@ def attn_chunk_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.floa
     return out, lse
 
 
+def attn_chunks_fwd(q, k, v, chunks, partials=None, lses=None, scale=None,
+                    partial_dtype=torch.float32, stream=None):
+    """Every chunk's partial (O_c, lse_c) of the ring decomposition in one launch
+    (dit_attn_chunks_fwd): chunk c is keys [s_c, s_c + chunks[c]) of k / v, s_c the sum of the
+    earlier lengths.  Returns (partials [p, B, H, N_q, D] of partial_dtype, lses [p, B, H, N_q])."""
+    _check_qkv(q, k, v)
+    B, H, Nq, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
+        raise ValueError("k/v must be [B, H, n_kv, D] matching q")
+    if any(int(n) < 1 for n in chunks) or sum(int(n) for n in chunks) > k.shape[2]:
+        raise ValueError("chunk lengths must be positive and fit in the keys")
+    hs = kv_head_stride(k)
+    if kv_head_stride(v) != hs:
+        raise ValueError("k and v must have the same head stride")
+    p = len(chunks)
+    starts = (ctypes.c_int * (p + 1))()
+    acc = 0
+    for c, n in enumerate(chunks):
+        starts[c] = acc
+        acc += int(n)
+    starts[p] = acc
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if partials is None:
+        partials = torch.empty((p, B, H, Nq, D), device=q.device, dtype=partial_dtype)
+    if lses is None:
+        lses = torch.empty((p, B, H, Nq), device=q.device, dtype=torch.float32)
+    if not partials.is_contiguous() or not lses.is_contiguous():
+        raise ValueError("partials and lses must be contiguous")
+    with torch.cuda.device(q.device):
+        st = lib().dit_attn_chunks_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(partials), _ptr(lses), B, H,
+                                       Nq, k.shape[2], D, hs, p, starts, scale, _dt(partials.dtype),
+                                       _stream(q.device, stream))
+    if st != DIT_OK:
+        raise DitError(st, "dit_attn_chunks_fwd")
+    return partials, lses
+
+
 def attn_chunk_fwd_accumulate(q, k, v, o_run, lse_run, scale=None, stream=None):
     """One ring hop with the merge fused in: the attention of q against one KV chunk (a view such
     as k[:, :, s:s+n] or a packed buffer) merged in place into the running o_run (fp32
@@ -465,9 +505,11 @@ def set_grid_limit(max_ctas: int):
 
 
 def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,
-                    partial_dtype=torch.float32, partials=None, lses=None, stream=None):
-    """Ring decomposition on one GPU: one dit_attn_chunk_fwd per KV chunk (virtual rank), then
-    one dit_attn_lse_merge.  `chunks` lists the chunk lengths (sum = N_kv)."""
+                    partial_dtype=torch.float32, partials=None, lses=None, stream=None,
+                    batched=False):
+    """Ring decomposition on one GPU: one dit_attn_chunk_fwd per KV chunk (virtual rank), or
+    with batched=True all chunks in one dit_attn_chunks_fwd launch (bitwise the same partials),
+    then one dit_attn_lse_merge.  `chunks` lists the chunk lengths (sum = N_kv)."""
     B, H, Nq, D = q.shape
     if sum(chunks) != k.shape[2]:
         raise ValueError("chunk lengths must sum to the number of keys")
@@ -476,11 +518,14 @@ def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,
         partials = torch.empty((p, B, H, Nq, D), device=q.device, dtype=partial_dtype)
     if lses is None:
         lses = torch.empty((p, B, H, Nq), device=q.device, dtype=torch.float32)
-    s = 0
-    for c, n in enumerate(chunks):
-        attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=partials[c], lse=lses[c],
-                       scale=scale, stream=stream)
-        s += n
+    if batched:
+        attn_chunks_fwd(q, k, v, chunks, partials=partials, lses=lses, scale=scale, stream=stream)
+    else:
+        s = 0
+        for c, n in enumerate(chunks):
+            attn_chunk_fwd(q, k[:, :, s:s + n], v[:, :, s:s + n], out=partials[c], lse=lses[c],
+                           scale=scale, stream=stream)
+            s += n
     return attn_lse_merge(partials, lses, out_dtype=out_dtype, stream=stream)
 
 

@@ -99,6 +99,31 @@ dit_status dit_attn_chunk_fwd(const void* q, const void* k, const void* v, void*
                               dit_stream stream);
 
 /*
+ * All virtual ranks of the ring decomposition in one launch: for each of p key
+ * chunks c = [chunk_starts[c], chunk_starts[c+1]) of k / v, the partial output and
+ * LSE of all N_q queries against that chunk alone, exactly as dit_attn_chunk_fwd
+ * defines them (a Ring round's local attention on the block a rank holds;
+ * arganzheng.life, section 4.2 Ring: one KV block per round, combined by online
+ * softmax).  Bitwise equal to p dit_attn_chunk_fwd calls on the chunk views; one
+ * persistent launch has no per-chunk launch gaps or tails.  dit_attn_lse_merge
+ * then combines the partials.
+ *   q, k, v, B, H, N_q, n_kv, D, kv_head_stride, scale : as dit_attn_chunk_fwd,
+ *                  k / v holding all n_kv key rows
+ *   partials     : device [p, B, H, N_q, D] of partial_dtype, contiguous, 16-byte
+ *                  aligned (written)
+ *   lses         : device fp32 [p, B, H, N_q], contiguous (written)
+ *   p            : 1 .. 64
+ *   chunk_starts : HOST array of p + 1 key-row offsets, 0 <= chunk_starts[0] <
+ *                  chunk_starts[1] < ... < chunk_starts[p] <= n_kv (read before the
+ *                  call returns; the chunks need not cover all keys)
+ * partials and lses must not overlap each other or q, k, v (DIT_ERR_INVALID_ARG).
+ */
+dit_status dit_attn_chunks_fwd(const void* q, const void* k, const void* v, void* partials,
+                               float* lses, int B, int H, int N_q, int n_kv, int D,
+                               long long kv_head_stride, int p, const int* chunk_starts,
+                               float scale, dit_dtype partial_dtype, dit_stream stream);
+
+/*
  * General-layout form of dit_attn_fwd / dit_attn_chunk_fwd: attention of N_q
  * queries against n_kv keys, each of q, k, v and out an arbitrary strided
  * [B, H, N, D] view (last dimension contiguous).  This reads and writes the

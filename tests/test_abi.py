@@ -97,6 +97,42 @@ def test_chunk_validation(lib, kw, status):
     assert chunk(lib, **kw) == status
 
 
+def chunks_batched(lib, starts=(0, 40, 100), n_kv=100, hs=256 * 128, D=128, p=None, **kw):
+    args = dict(q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, scale=0.088, dt=0)
+    args.update(kw)
+    p = len(starts) - 1 if p is None else p
+    arr = (ctypes.c_int * max(1, len(starts)))(*starts) if starts is not None else None
+    return lib.dit_attn_chunks_fwd(args["q"], args["k"], args["v"], args["out"], args["lse"],
+                                   args["B"], args["H"], args["N"], n_kv, D, hs, p, arr,
+                                   args["scale"], args["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(starts=None, p=2), da.DIT_ERR_INVALID_ARG),                 # no chunk table
+    (dict(starts=(0,), p=0), da.DIT_ERR_INVALID_ARG),                 # p = 0
+    (dict(starts=tuple(range(66)), n_kv=100, p=65), da.DIT_ERR_INVALID_ARG),   # p > 64
+    (dict(starts=(0, 40, 40)), da.DIT_ERR_INVALID_ARG),               # empty chunk
+    (dict(starts=(0, 60, 40)), da.DIT_ERR_INVALID_ARG),               # decreasing
+    (dict(starts=(-1, 40, 100)), da.DIT_ERR_INVALID_ARG),             # before the first key
+    (dict(starts=(0, 40, 101)), da.DIT_ERR_INVALID_ARG),              # past n_kv
+    (dict(n_kv=0), da.DIT_ERR_INVALID_ARG), (dict(D=96), da.DIT_ERR_UNSUPPORTED),
+    (dict(dt=5), da.DIT_ERR_INVALID_ARG),
+    # the second partial block (256 rows x 2 heads x 128 x 4 B past OUT) would overlap LSE
+    (dict(lse=ctypes.c_void_p((4 << 40) + 2 * 256 * 128 * 4 + 256)), da.DIT_ERR_INVALID_ARG),
+    # the second chunk's LSE rows overlap a partial block placed right after them
+    (dict(out=ctypes.c_void_p((5 << 40) + 2 * 256 * 4 + 256)), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((2 << 40) + 64)), da.DIT_ERR_INVALID_ARG),     # partials inside k
+])
+def test_chunks_batched_validation(lib, kw, status):
+    assert chunks_batched(lib, **kw) == status
+
+
+def test_chunks_batched_binding_rejects_host_tensors():
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        da.attn_chunks_fwd(x, x, x, [4, 4])
+
+
 def accumulate(lib, n_kv=100, hs=256 * 128, D=128, **kw):
     args = dict(q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, scale=0.088)
     args.update(kw)
