@@ -7,15 +7,16 @@
 // (MindIE-SD parallelism docs, "Ring Sequence Parallel" usage example: local
 // attention; arganzheng.life multi-GPU diffusion parallelism, section 4.2 Ring:
 // one KV block per round, combined by online softmax).  The same kernel serves
-// the fused pass (n_kv = N), one KV chunk of the ring decomposition, the ring hop
-// merged into a running (O, lse) (kAccum), and split-KV partials.  Q/K/V are read
+// the fused pass (n_kv = N), one KV chunk of the ring decomposition, all p chunks
+// (virtual ranks) in one launch, the ring hop merged into a running (O, lse)
+// (kAccum), and split-KV partials.  Q/K/V are read
 // through 4-D tensor maps (d, rows, heads, batch) with any strides, O is written
 // through per-head offsets and a row stride, so token-major (BSND) views work too.
 //
 // Persistent: one CTA per SM walks work items (head bh, pair of 128-row Q tiles,
 // key range) w = blockIdx.x, blockIdx.x + gridDim.x, ...  (head-major, so the CTAs
 // resident at any moment share a head's K/V in L2; the key range is the whole key
-// set unless split-KV).  Every barrier's phase count runs on across items, so the
+// set, a tile-aligned split, or one chunk at any row offset).  Every barrier's phase count runs on across items, so the
 // next item's Q load and first S MMAs overlap this item's epilogue.
 //
 // CTA organisation (512 threads, four warpgroups):
