@@ -550,16 +550,27 @@ def ring_attention(q, k, v, chunks, scale=None, o_run=None, lse_run=None, stream
     return o_run, lse_run
 
 
-def head_groups(n_heads, groups=3):
+def head_groups(n_heads, groups=5):
     """Split n_heads heads into consecutive groups for host pipelining: small first and last
-    groups (so the first compute starts, and the last copy-back ends, early) around a large
-    middle one.  Returns [(h0, h1), ...]."""
-    if n_heads < 3 or groups < 3:
-        if n_heads < 2 or groups < 2:
-            return [(0, n_heads)]
-        return [(0, n_heads // 2), (n_heads // 2, n_heads)]
-    edge = max(1, n_heads // 6)
-    return [(0, edge), (edge, n_heads - edge), (n_heads - edge, n_heads)]
+    groups (so that the first compute starts, and the last copy-back ends, early) around a
+    large middle one.  groups=5 (the default) gives about 1/12, 1/6, 1/2, 1/6, 1/12 of the
+    heads (2, 4, 12, 4, 2 for 24 heads: the fastest end-to-end split measured for the Wan2.2
+    shape among eight tried); groups=3 gives about 1/6, 2/3, 1/6.  Returns [(h0, h1), ...]."""
+    if groups >= 5 and n_heads >= 5:
+        e1, e2 = max(1, n_heads // 12), max(1, n_heads // 6)
+        sizes = [e1, e2, n_heads - 2 * (e1 + e2), e2, e1]
+    elif groups >= 3 and n_heads >= 3:
+        edge = max(1, n_heads // 6)
+        sizes = [edge, n_heads - 2 * edge, edge]
+    elif groups >= 2 and n_heads >= 2:
+        sizes = [n_heads // 2, n_heads - n_heads // 2]
+    else:
+        sizes = [n_heads]
+    out, h = [], 0
+    for n in sizes:
+        out.append((h, h + n))
+        h += n
+    return out
 
 
 _PIPE_STREAMS = {}

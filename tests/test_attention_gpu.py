@@ -410,7 +410,7 @@ def test_host_tensors_pipelined_over_head_groups(pinned):
     q, k, v = rand_qkv(B, H, N, D, seed=91)
     if pinned:
         q, k, v = q.pin_memory(), k.pin_memory(), v.pin_memory()
-    assert da.head_groups(B * H) == [(0, 2), (2, 12), (12, 14)]
+    assert da.head_groups(B * H) == [(0, 1), (1, 3), (3, 11), (11, 13), (13, 14)]
     qd, kd, vd = to_dev(q, k, v)
     chunks = [200, 150, 250]
     for kw in (dict(), dict(chunks=chunks), dict(chunks=chunks, accumulate=True),
