@@ -5,7 +5,9 @@ Every case draws B, H, D, the query and key counts (ragged, from 1 row up), the 
 and, where the entry point has them, a random chunk split, split-KV count or patch position;
 the case list is fixed by the seed, so a failure names a reproducible configuration.
 Tolerances are those of the other parity tests: max-abs 1e-2, mean-abs 1e-3, LSE 1e-3 (a bf16
-output is allowed one bf16 ulp of the oracle value where that is larger).
+output is allowed one bf16 ulp of the oracle value where that is larger; a merge of bf16
+partials, one bf16 ulp of each partial weighted by its merge weight, from the oracle's own
+partials, where that is larger).
 """
 import math
 
@@ -21,10 +23,10 @@ pytestmark = pytest.mark.gpu
 MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 1e-3
 DEV = torch.device("cuda:0")
 PATHS = ("fused", "fused_bf16", "chunks_f32", "chunks_bf16", "ring", "splitkv", "bsnd",
-         "cross", "stale")
+         "batched", "cross", "stale")
 
 
-def _cases(n=90, seed=2026):
+def _cases(n=100, seed=2026):
     rs = np.random.RandomState(seed)
     out = []
     for i in range(n):
@@ -32,10 +34,11 @@ def _cases(n=90, seed=2026):
         B, H = int(rs.randint(1, 3)), int(rs.randint(1, 4))
         D = int(rs.choice([64, 128]))
         nq = int(rs.choice([rs.randint(1, 130), rs.randint(1, 1400)]))
-        nk = nq if path in PATHS[:7] else int(rs.randint(1, 3000))
+        nk = nq if path in PATHS[:8] else int(rs.randint(1, 3000))
         if path == "stale":
             nk = max(nk, nq)
-        amp = float(rs.choice([0.5, 1.0, 2.0] if path == "chunks_bf16" else [0.5, 1.0, 2.0, 3.0]))
+        amp = float(rs.choice([0.5, 1.0, 2.0] if path in ("chunks_bf16", "batched")
+                              else [0.5, 1.0, 2.0, 3.0]))
         p = int(rs.randint(1, min(6, nk) + 1))
         cuts = np.sort(rs.choice(np.arange(1, nk), size=p - 1, replace=False)) if p > 1 else []
         chunks = tuple(int(x) for x in np.diff(np.concatenate([[0], cuts, [nk]])))
@@ -54,11 +57,25 @@ def _ulp_bf16(x):
     return np.power(2.0, np.floor(np.log2(np.maximum(a, 1e-30))) - 7)
 
 
-def _check(o, lse, o_ref, lse_ref, what, bf16_out=False):
+def _bf16_partials_bound(q, k, v, scale, chunks, lse_ref):
+    """Error a merge of bf16-rounded partials may carry: each partial O_c is rounded once to
+    bf16 (up to half an ulp of O_c), and the merge weights it by exp(lse_c - lse); one full
+    ulp per partial is allowed.  The partials and weights come from the oracle."""
+    bound, s = 0.0, 0
+    for n in chunks:
+        oc, lc = oracle.attention(q, k, v, scale, kv_start=s, kv_len=n)
+        bound = bound + np.exp(lc - lse_ref)[..., None] * _ulp_bf16(oc)
+        s += n
+    return bound
+
+
+def _check(o, lse, o_ref, lse_ref, what, bf16_out=False, extra_bound=None):
     o = o.detach().double().cpu().numpy()
     lse = lse.detach().double().cpu().numpy()
     err = np.abs(o - o_ref)
     bound = np.maximum(MAX_ABS, _ulp_bf16(o_ref)) if bf16_out else MAX_ABS
+    if extra_bound is not None:
+        bound = np.maximum(bound, extra_bound)
     assert (err <= bound).all(), f"{what}: max-abs {err.max():.3e}"
     assert err.mean() <= MEAN_ABS, f"{what}: mean-abs {err.mean():.3e}"
     lerr = np.abs(lse - lse_ref).max()
@@ -96,6 +113,7 @@ def test_random_case(case):
 
     o_ref, lse_ref = oracle.attention(q, k, v, scale)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    extra = None
     if path == "fused":
         o, lse = da.attn_fwd(qd, kd, vd, scale=scale)
     elif path == "fused_bf16":
@@ -105,11 +123,18 @@ def test_random_case(case):
     elif path == "chunks_bf16":
         o, lse = da.chunk_attention(qd, kd, vd, c["chunks"], scale=scale,
                                     partial_dtype=torch.bfloat16)
+        extra = _bf16_partials_bound(q, k, v, scale, c["chunks"], lse_ref)
     elif path == "ring":
         o, lse = da.ring_attention(qd, kd, vd, c["chunks"], scale=scale)
     elif path in ("splitkv", "cross"):
         splits = min(c["splits"], (nk + 127) // 128) if path == "splitkv" else None
         o, lse = da.attn_chunk_fwd_splitkv(qd, kd, vd, scale=scale, splits=splits)
+    elif path == "batched":
+        partial_dtype = torch.bfloat16 if c["seed"] % 2 else torch.float32
+        o, lse = da.chunk_attention(qd, kd, vd, c["chunks"], scale=scale, batched=True,
+                                    partial_dtype=partial_dtype)
+        if partial_dtype == torch.bfloat16:
+            extra = _bf16_partials_bound(q, k, v, scale, c["chunks"], lse_ref)
     elif path == "bsnd":
         qs, ks, vs = (x.transpose(1, 2).contiguous().transpose(1, 2) for x in (qd, kd, vd))
         out = torch.empty(B, nq, H, D, device=DEV).transpose(1, 2)
@@ -117,4 +142,4 @@ def test_random_case(case):
     else:
         raise AssertionError(path)
     da.check()
-    _check(o, lse, o_ref, lse_ref, what, bf16_out=(path == "fused_bf16"))
+    _check(o, lse, o_ref, lse_ref, what, bf16_out=(path == "fused_bf16"), extra_bound=extra)
