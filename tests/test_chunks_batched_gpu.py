@@ -105,3 +105,42 @@ def test_wan22_size_batched_equals_per_chunk():
     pc, lc = per_chunk(qd, kd, vd, w.chunks, w.scale, torch.float32)
     da.check()
     assert torch.equal(pb, pc) and torch.equal(lb, lc)
+
+
+@pytest.mark.parametrize("p", [1, 64])
+def test_chunk_count_limits(p):
+    D, nk = 64, 700
+    q, k, v = rand_qkv(1, 2, 150, nk, D, seed=p)
+    scale = 1 / math.sqrt(D)
+    base, rem = divmod(nk, p)
+    chunks = [base + (1 if c < rem else 0) for c in range(p)]
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    pb, lb = da.attn_chunks_fwd(qd, kd, vd, chunks, scale=scale)
+    pc, lc = per_chunk(qd, kd, vd, chunks, scale, torch.float32)
+    o, lse = da.attn_lse_merge(pb, lb)
+    da.check()
+    assert torch.equal(pb, pc) and torch.equal(lb, lc)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    check(o, lse, o_ref, lse_ref, f"p={p}")
+
+
+def test_chunk_table_not_starting_at_key_zero():
+    """The C ABI takes any increasing table inside [0, n_kv]: chunks [100, 400) and
+    [400, 650) of 700 keys."""
+    import ctypes
+    D, nk = 128, 700
+    q, k, v = rand_qkv(2, 1, 300, nk, D, seed=5)
+    scale = 1 / math.sqrt(D)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    parts = torch.empty(2, 2, 1, 300, D, device=DEV)
+    lses = torch.empty(2, 2, 1, 300, device=DEV)
+    starts = (ctypes.c_int * 3)(100, 400, 650)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = da.lib().dit_attn_chunks_fwd(ptr(qd), ptr(kd), ptr(vd), ptr(parts), ptr(lses), 2, 1, 300,
+                                      nk, D, nk * D, 2, starts, scale, 0,
+                                      ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == da.DIT_OK
+    o, lse = da.attn_lse_merge(parts, lses)
+    da.check()
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, kv_start=100, kv_len=550)
+    check(o, lse, o_ref, lse_ref, "chunks over keys [100, 650)")
