@@ -423,6 +423,16 @@ def run_gpu(args):
     per_rank_ms = timed(chunk_per_rank)
     del parts16
 
+    # ---- the fused pass without the LSE output (O only; bitwise the same O) ----
+    out_nl = torch.empty_like(out_f)
+
+    def fused_no_lse():
+        da.attn_fwd(q, k, v, out=out_nl, scale=w.scale, with_lse=False)
+
+    no_lse_ms = timed(fused_no_lse)
+    no_lse_same = bool(torch.equal(out_nl, out_f))
+    del out_nl
+
     # ---- hop-by-hop ring: each chunk pass merges into the running (O, lse) itself ----
     # The first hop writes the running state (dit_attn_chunk_fwd, fp32), the other p-1 fold
     # their chunk in (dit_attn_chunk_fwd_accumulate): no stacked partials, no merge pass.
@@ -621,6 +631,9 @@ def run_gpu(args):
                 "chunk_merge_bf16_partials": {"ms": chunk16_ms,
                                               **tf_frac(w.flops / (chunk16_ms * 1e-3) / 1e12),
                                               "ratio_to_fused": chunk16_ms / fused_ms},
+                "fused_without_lse": {"ms": no_lse_ms,
+                                      **tf_frac(w.flops / (no_lse_ms * 1e-3) / 1e12),
+                                      "o_bitwise_equal": no_lse_same},
                 "chunk_merge_per_rank_launches": {
                     "ms": per_rank_ms, **tf_frac(w.flops / (per_rank_ms * 1e-3) / 1e12),
                     "ratio_to_fused": per_rank_ms / fused_ms, "launches": p + 1},

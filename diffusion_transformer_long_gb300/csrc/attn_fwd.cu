@@ -68,10 +68,10 @@ bool encode_view(CUtensorMap* m, const void* base, int d, int rows, int heads, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kF32, bool kAccum = false>
+template <int D, bool kF32, bool kAccum = false, bool kLse = true>
 cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
   constexpr int kSmem = AttnSmem<D>::kBytes;
-  auto kern = attn_fwd_kernel<D, kF32, kAccum>;
+  auto kern = attn_fwd_kernel<D, kF32, kAccum, kLse>;
   // The shared-memory opt-in is set once per device and instantiation, so that later
   // launches are only the launch itself.
   static std::mutex mu;
@@ -111,6 +111,7 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   if (split && (a.accumulate || batched || !a.ws_o || !a.ws_lse)) return cudaErrorInvalidValue;
   if (batched && (a.accumulate || a.chunks > kMaxRanges || !a.chunk_starts))
     return cudaErrorInvalidValue;
+  if (!a.lse && (a.accumulate || split || batched)) return cudaErrorInvalidValue;
   // Split-KV passes write fp32 partials, contiguous, into the workspace.
   const bool f32 = split || a.out_f32;
   void* const obase = split ? static_cast<void*>(a.ws_o) : a.out;
@@ -165,6 +166,13 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
     m.part_f32 = true;
     m.out_f32 = a.out_f32;
     return launch_merge(m, st);
+  }
+  if (!a.lse) {  // no LSE output (one key range; checked above)
+    if (a.d == 64)
+      return a.out_f32 ? launch_typed<64, true, false, false>(prm, st)
+                       : launch_typed<64, false, false, false>(prm, st);
+    return a.out_f32 ? launch_typed<128, true, false, false>(prm, st)
+                     : launch_typed<128, false, false, false>(prm, st);
   }
   if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
   return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);

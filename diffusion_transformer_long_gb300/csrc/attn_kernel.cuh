@@ -495,7 +495,7 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
       : "r"(w));
 }
 
-template <int D, bool kAccum>
+template <int D, bool kAccum, bool kLse>
 __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                            int t, int warp, int lane,
                                            volatile int* abort_flag) {
@@ -634,7 +634,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
           for (int q = 0; q < 4; ++q) {
             const float p0 = s[8 * ch + 2 * q], p1 = s[8 * ch + 2 * q + 1];
             wv[q] = ptx::pack_bf16x2(p0, p1);
-            acc_l[q] = ptx::fadd2(acc_l[q], ptx::f2pack(p0, p1));
+            if constexpr (kLse) acc_l[q] = ptx::fadd2(acc_l[q], ptx::f2pack(p0, p1));
             add_bf16x2(acc_lp[2 * q], acc_lp[2 * q + 1], wv[q]);
           }
           const uint32_t addr = sP + half * L::kRegion + r * 128 +
@@ -650,11 +650,13 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       if (!ok) break;
       if (r == 0) DIT_TRACE(kTrSmArrive0 + 5 * t, g);
       {
-        const uint64_t sl =
-            ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
-        float a0, a1;
-        ptx::f2unpack(sl, a0, a1);
-        l += a0 + a1;
+        if constexpr (kLse) {
+          const uint64_t sl =
+              ptx::fadd2(ptx::fadd2(acc_l[0], acc_l[1]), ptx::fadd2(acc_l[2], acc_l[3]));
+          float a0, a1;
+          ptx::f2unpack(sl, a0, a1);
+          l += a0 + a1;
+        }
         lp += ((acc_lp[0] + acc_lp[1]) + (acc_lp[2] + acc_lp[3])) +
               ((acc_lp[4] + acc_lp[5]) + (acc_lp[6] + acc_lp[7]));
       }
@@ -674,7 +676,12 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
       hand[t * kBlockM + r] = 1.f / lp;
       ptx::mbar_arrive(bar(L::bEpiReady + t));
-      if (row < p.n_q) *lse_row = lse2 * kLn2;
+      if constexpr (kLse) {
+        if (row < p.n_q) *lse_row = lse2 * kLn2;
+      } else {
+        (void)lse_row;
+        (void)lse2;
+      }
     } else {
       // Accumulate mode: the epilogue merges this pass into the running (O, lse); it gets
       // (this pass's LSE in log2 units, 1 / lp) through one slot [r][2] shared by both Q
@@ -911,8 +918,10 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
 
 }  // namespace detail
 
-template <int D, bool kOutF32, bool kAccum>
+// kLse = false: no LSE output (p.lse unused) and no unrounded row sum; O is unchanged.
+template <int D, bool kOutF32, bool kAccum, bool kLse = true>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(kLse || !kAccum, "the running merge needs the LSE");
   using L = AttnSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -962,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
   if (warp < kLoadWarp) {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
-    detail::softmax_wg<D, kAccum>(p, sbase, tmem, warp >> 2, warp, lane, abort_flag);
+    detail::softmax_wg<D, kAccum, kLse>(p, sbase, tmem, warp >> 2, warp, lane, abort_flag);
   } else if (warp < kEpiWarp0) {
     ptx::setmaxnreg_dec<kRegsIssue>();
     if (warp == kLoadWarp) {

@@ -58,11 +58,12 @@ dit_status check_dims(long long B, long long H, long long N, int D) {
 
 dit_status validate_attention(const void* q, const void* k, const void* v, const void* out,
                               const float* lse, int B, int H, int N_q, int n_kv, int D,
-                              long long kv_head_stride, float scale, dit_dtype out_dtype) {
+                              long long kv_head_stride, float scale, dit_dtype out_dtype,
+                              bool lse_optional = false) {
   dit_status s = check_dims(B, H, N_q, D);
   if (s != DIT_OK) return s;
   if (n_kv < 1) return DIT_ERR_INVALID_ARG;
-  if (!q || !k || !v || !out || !lse) return DIT_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || (!lse && !lse_optional)) return DIT_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
       !aligned(lse, 4))
     return DIT_ERR_INVALID_ARG;
@@ -79,7 +80,7 @@ dit_status validate_attention(const void* q, const void* k, const void* v, const
   const long long kv_bytes = ((bh - 1) * kv_head_stride + static_cast<long long>(n_kv) * D) * 2;
   const Range rk = span(k, kv_bytes), rv = span(v, kv_bytes);
   const Range ro = span(out, qkv_rows * D * dtype_bytes(out_dtype));
-  const Range rl = span(lse, qkv_rows * 4);
+  const Range rl = span(lse, lse ? qkv_rows * 4 : 0);
   for (Range in : {rq, rk, rv})
     if (overlap(ro, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
   if (overlap(ro, rl)) return DIT_ERR_INVALID_ARG;
@@ -205,7 +206,8 @@ extern "C" {
 dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                         int H, int N, int D, float scale, dit_dtype out_dtype, dit_stream stream) {
   const long long hs = static_cast<long long>(N) * D;
-  dit_status s = validate_attention(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype);
+  dit_status s = validate_attention(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype,
+                                    /*lse_optional=*/true);
   if (s != DIT_OK) return s;
   return run_contiguous(q, k, v, out, lse, B, H, N, N, D, hs, scale, out_dtype, stream);
 }
@@ -264,7 +266,7 @@ dit_status dit_attn_fwd_strided(const void* q, const dit_strides* q_strides, con
   dit_status s = check_dims(B, H, N_q, D);
   if (s != DIT_OK) return s;
   if (n_kv < 1 || n_kv > INT_MAX) return DIT_ERR_INVALID_ARG;
-  if (!q || !k || !v || !out || !lse) return DIT_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out) return DIT_ERR_INVALID_ARG;  // lse may be NULL
   if (!valid_dtype(out_dtype)) return DIT_ERR_INVALID_ARG;
   if (!(scale > 0.f) || !std::isfinite(scale)) return DIT_ERR_INVALID_ARG;
   // The stride of a size-1 dimension addresses nothing: any valid value will do.
@@ -289,7 +291,7 @@ dit_status dit_attn_fwd_strided(const void* q, const dit_strides* q_strides, con
   const Range rk = span(k, view_span(ks, B, H, n_kv, D, 2));
   const Range rv = span(v, view_span(vs, B, H, n_kv, D, 2));
   const Range ro = span(out, view_span(os, B, H, N_q, D, oes));
-  const Range rl = span(lse, bh * N_q * 4);
+  const Range rl = span(lse, lse ? bh * N_q * 4 : 0);
   for (Range in : {rq, rk, rv})
     if (overlap(ro, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
   if (overlap(ro, rl)) return DIT_ERR_INVALID_ARG;

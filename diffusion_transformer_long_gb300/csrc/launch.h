@@ -17,7 +17,7 @@ struct AttnLaunch {
   const void* k;
   const void* v;
   void* out;
-  float* lse;                // contiguous [B, H, N_q]
+  float* lse;                // contiguous [B, H, N_q]; null: no LSE output (one key range)
   int* status;               // device status word
   int batch;                 // B
   int heads;                 // H

@@ -131,10 +131,12 @@ def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
-def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, stream=None):
+def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, stream=None,
+             with_lse=True):
     """Fused attention over all keys.  q, k, v: CUDA bf16 [B, H, N, D] contiguous.
 
-    Returns (out [B, H, N, D] of out_dtype, lse fp32 [B, H, N]).
+    Returns (out [B, H, N, D] of out_dtype, lse fp32 [B, H, N]); with_lse=False skips the
+    LSE (the library gets NULL) and returns (out, None).
     """
     _check_qkv(q, k, v)
     if not (k.is_contiguous() and v.is_contiguous()) or k.shape != q.shape or v.shape != q.shape:
@@ -143,14 +145,15 @@ def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, s
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty((B, H, N, D), device=q.device, dtype=out_dtype)
-    if lse is None:
+    if lse is None and with_lse:
         lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
     with torch.cuda.device(q.device):
-        st = lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, D,
-                                scale, _dt(out.dtype), _stream(q.device, stream))
+        st = lib().dit_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                _ptr(lse) if with_lse else None, B, H, N, D, scale,
+                                _dt(out.dtype), _stream(q.device, stream))
     if st != DIT_OK:
         raise DitError(st, "dit_attn_fwd")
-    return out, lse
+    return out, (lse if with_lse else None)
 
 
 def view_strides(x: torch.Tensor) -> Strides:

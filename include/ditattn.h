@@ -69,7 +69,8 @@ typedef struct {
  * section 4.1 Ulysses (full attention per head over all N tokens).
  *   q, k, v : device bf16 [B, H, N, D], contiguous, 16-byte aligned (read only)
  *   out     : device [B, H, N, D] of out_dtype (written)
- *   lse     : device fp32 [B, H, N] (written)
+ *   lse     : device fp32 [B, H, N] (written), or NULL when the caller needs only O:
+ *             the pass then skips the LSE and its unrounded row sum (O is the same)
  *   scale   : score scale, usually 1/sqrt(D)
  */
 dit_status dit_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -133,7 +134,8 @@ dit_status dit_attn_chunks_fwd(const void* q, const void* k, const void* v, void
  * and heads kept whole) directly, with no transpose.
  *   q, k, v     : device bf16 views; NULL strides = contiguous BHND
  *   out         : device view of out_dtype (written); NULL strides = contiguous
- *   lse         : device fp32 [B, H, N_q], contiguous (written)
+ *   lse         : device fp32 [B, H, N_q], contiguous (written), or NULL (no LSE,
+ *                 as for dit_attn_fwd)
  * Strides must be positive multiples of 8 elements (16-byte TMA strides) below
  * 2^39; out must not map two elements to one address; out and lse must not
  * overlap the address range of q, k or v (DIT_ERR_INVALID_ARG otherwise).

@@ -61,7 +61,7 @@ def fwd(lib, q=Q, k=K, v=V, out=OUT, lse=LSE, B=1, H=2, N=256, D=128, scale=0.08
     (dict(B=0), da.DIT_ERR_INVALID_ARG), (dict(H=-1), da.DIT_ERR_INVALID_ARG),
     (dict(N=0), da.DIT_ERR_INVALID_ARG), (dict(D=0), da.DIT_ERR_INVALID_ARG),
     (dict(D=96), da.DIT_ERR_UNSUPPORTED), (dict(D=256), da.DIT_ERR_UNSUPPORTED),
-    (dict(q=None), da.DIT_ERR_INVALID_ARG), (dict(lse=None), da.DIT_ERR_INVALID_ARG),
+    (dict(q=None), da.DIT_ERR_INVALID_ARG), (dict(out=None), da.DIT_ERR_INVALID_ARG),
     (dict(k=ctypes.c_void_p((2 << 40) + 8)), da.DIT_ERR_INVALID_ARG),
     (dict(out=ctypes.c_void_p((4 << 40) + 4)), da.DIT_ERR_INVALID_ARG),
     (dict(lse=ctypes.c_void_p((5 << 40) + 2)), da.DIT_ERR_INVALID_ARG),
@@ -86,6 +86,7 @@ def chunk(lib, n_kv=100, hs=256 * 128, D=128, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(n_kv=0), da.DIT_ERR_INVALID_ARG),
+    (dict(lse=None), da.DIT_ERR_INVALID_ARG),                 # a chunk's LSE is its output
     (dict(n_kv=300, hs=256 * 128), da.DIT_ERR_INVALID_ARG),   # stride shorter than the chunk
     (dict(hs=256 * 128 + 4), da.DIT_ERR_INVALID_ARG),         # stride not 16-byte aligned
     (dict(hs=1 << 39), da.DIT_ERR_INVALID_ARG),

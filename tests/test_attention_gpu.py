@@ -455,3 +455,31 @@ def test_extreme_logits_every_path(amp):
         assert (lerr <= 1e-3 + 16 * ulp).all(), f"amp {amp} {name}: lse {lerr.max():.3e}"
         err = np.abs(o.double().cpu().numpy() - o_ref)
         assert err.max() <= MAX_ABS and err.mean() <= MEAN_ABS, f"amp {amp} {name}: {err.max()}"
+
+
+@pytest.mark.parametrize("D,dtype", [(64, torch.float32), (128, torch.float32),
+                                     (64, torch.bfloat16), (128, torch.bfloat16)])
+def test_fused_without_lse(D, dtype):
+    """lse = NULL: the pass skips the LSE and its unrounded row sum; O is bitwise the same
+    (it is normalised by the rounded sum either way), on the plain and strided entry points."""
+    q, k, v = rand_qkv(2, 3, 517, D, seed=D + 3, scale=1.5)
+    scale = 1 / math.sqrt(D)
+    qd, kd, vd = to_dev(q, k, v)
+    o1, l1 = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=dtype)
+    o2, l2 = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=dtype, with_lse=False)
+    q_s, k_s, v_s = (da.bhnd_to_bsnd(t) for t in (qd, kd, vd))
+    o3 = torch.empty(2, 517, 3, D, device=DEV, dtype=dtype).transpose(1, 2)
+    with torch.cuda.device(DEV):
+        qs, ks, vs, os_ = (da.view_strides(t) for t in (q_s.transpose(1, 2), k_s.transpose(1, 2),
+                                                         v_s.transpose(1, 2), o3))
+        import ctypes
+        st = da.lib().dit_attn_fwd_strided(
+            ctypes.c_void_p(q_s.data_ptr()), ctypes.byref(qs), ctypes.c_void_p(k_s.data_ptr()),
+            ctypes.byref(ks), ctypes.c_void_p(v_s.data_ptr()), ctypes.byref(vs),
+            ctypes.c_void_p(o3.data_ptr()), ctypes.byref(os_), None, 2, 3, 517, 517, D, scale,
+            0 if dtype == torch.float32 else 1,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == da.DIT_OK
+    da.check()
+    assert l2 is None
+    assert torch.equal(o1, o2) and torch.equal(o1, o3)
