@@ -620,12 +620,15 @@ def host_pipeline(fn, inputs, outputs, groups, device=None):
 
 
 def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
-              partial_dtype=torch.float32, device=None, accumulate=False):
+              partial_dtype=torch.float32, device=None, accumulate=False, with_lse=True):
     """User-level call.  Accepts CUDA tensors, or CPU tensors (pinned for the copies to overlap)
     that are processed in head groups through host_pipeline, results returned in pinned host
     memory.  chunks=None runs the fused pass; a list of chunk lengths runs the p-chunk ring
     decomposition, merged by a separate LSE-merge pass or, with accumulate=True, hop by hop
-    inside each chunk pass (fp32 output)."""
+    inside each chunk pass (fp32 output).  with_lse=False (fused pass on device tensors only)
+    skips the LSE and returns (out, None)."""
+    if not with_lse and (chunks is not None or not q.is_cuda):
+        raise ValueError("with_lse=False applies to the fused pass on device tensors")
     if not q.is_cuda:
         # Host tensors: pipelined over head groups (uploads, compute and downloads overlap).
         B, H, Nq, D = q.shape
@@ -643,7 +646,7 @@ def attention(q, k, v, scale=None, chunks=None, out_dtype=torch.float32,
         host_pipeline(per_group, flat, [out_h, lse_h], head_groups(B * H), device)
         return out_h.view(B, H, Nq, D), lse_h.view(B, H, Nq)
     if chunks is None:
-        out, lse = attn_fwd(q, k, v, scale=scale, out_dtype=out_dtype)
+        out, lse = attn_fwd(q, k, v, scale=scale, out_dtype=out_dtype, with_lse=with_lse)
     elif accumulate:
         if out_dtype != torch.float32:
             raise ValueError("the hop-by-hop ring accumulates in fp32")
