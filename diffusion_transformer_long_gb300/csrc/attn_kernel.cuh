@@ -627,6 +627,8 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
           // The P_t buffer is free once PV_t(g-1) has read it.
           if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
         }
+        // Pack to bf16 and store row r of this half's swizzled region; accumulate the row
+        // sums (unrounded for the LSE, bf16-rounded for O) in independent chains.
 #pragma unroll
         for (int ch = half * 8; ch < half * 8 + 8; ++ch) {
           uint32_t wv[4];
