@@ -16,8 +16,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libditattn.so")
-SOURCES = ["attn_fwd.cu", "lse_merge.cu", "layout_copy.cu", "noalloc.cu", "ditattn_api.cu"]
-HEADERS = ["attn_kernel.cuh", "sm103_ptx.cuh", "launch.h"]
+SOURCES = ["attn_fwd.cu", "attn_fwd_short.cu", "lse_merge.cu", "layout_copy.cu", "noalloc.cu", "ditattn_api.cu"]
+HEADERS = ["attn_kernel.cuh", "attn_host.cuh", "merge_math.cuh", "sm103_ptx.cuh", "launch.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -2,10 +2,11 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
-#include "attn_kernel.cuh"
+#include "attn_host.cuh"
 #include "launch.h"
 
 namespace ditattn {
@@ -16,20 +17,6 @@ int g_stall_kv = 0;
 long long g_wait_limit = kDefaultWaitLimit;
 // Test-only cap on the persistent grid (0: one CTA per SM).
 int g_grid_limit = 0;
-
-// Streaming multiprocessors of the current device, cached per device.
-int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
-      n = 1;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -66,36 +53,6 @@ bool encode_view(CUtensorMap* m, const void* base, int d, int rows, int heads, i
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
             elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int D, bool kF32, bool kAccum = false, bool kLse = true>
-cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st) {
-  constexpr int kSmem = AttnSmem<D>::kBytes;
-  auto kern = attn_fwd_kernel<D, kF32, kAccum, kLse>;
-  // The shared-memory opt-in is set once per device and instantiation, so that later
-  // launches are only the launch itself.
-  static std::mutex mu;
-  static bool done[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
-      if (e != cudaSuccess) return e;
-      done[dev] = true;
-    }
-  }
-  // Persistent grid: one CTA per SM (shared memory and TMEM allow no more), each
-  // walking work items blockIdx.x, blockIdx.x + gridDim.x, ...
-  int ctas = sm_count();
-  if (g_grid_limit > 0 && g_grid_limit < ctas) ctas = g_grid_limit;
-  if (prm.num_items < ctas) ctas = prm.num_items;
-  const dim3 grid(static_cast<unsigned>(ctas));
-  kern<<<grid, kThreads, kSmem, st>>>(prm);
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -148,12 +105,26 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   prm.scale_log2 = a.scale * 1.4426950408889634f;
   prm.wait_limit = g_wait_limit;
   prm.stall_kv = g_stall_kv;
+  // KV tiles of the longest work item: short items take the soft-drain form.
+  int item_tiles = prm.tiles_total;
+  if (batched) {
+    item_tiles = 0;
+    for (int c = 0; c < a.chunks; ++c)
+      item_tiles = std::max(item_tiles, (a.chunk_starts[c + 1] - a.chunk_starts[c] + kBlockN - 1) /
+                                            kBlockN);
+  } else if (split) {
+    item_tiles = (prm.tiles_total + a.splits - 1) / a.splits;
+  }
+  const bool short_items = item_tiles <= host::kShortItemTiles;
   if (a.accumulate) {
     if (!a.out_f32) return cudaErrorInvalidValue;
-    return a.d == 64 ? launch_typed<64, true, true>(prm, st) : launch_typed<128, true, true>(prm, st);
+    return a.d == 64 ? host::launch_typed<64, true, true>(prm, st, g_grid_limit)
+                     : host::launch_typed<128, true, true>(prm, st, g_grid_limit);
   }
   if (split) {
-    const cudaError_t e = a.d == 64 ? launch_typed<64, true>(prm, st) : launch_typed<128, true>(prm, st);
+    const cudaError_t e = short_items ? host::launch_short(prm, a.d, true, st, g_grid_limit)
+                          : a.d == 64 ? host::launch_typed<64, true>(prm, st, g_grid_limit)
+                                      : host::launch_typed<128, true>(prm, st, g_grid_limit);
     if (e != cudaSuccess) return e;
     MergeLaunch m;
     m.partials = a.ws_o;
@@ -169,13 +140,17 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   }
   if (!a.lse) {  // no LSE output (one key range; checked above)
     if (a.d == 64)
-      return a.out_f32 ? launch_typed<64, true, false, false>(prm, st)
-                       : launch_typed<64, false, false, false>(prm, st);
-    return a.out_f32 ? launch_typed<128, true, false, false>(prm, st)
-                     : launch_typed<128, false, false, false>(prm, st);
+      return a.out_f32 ? host::launch_typed<64, true, false, false>(prm, st, g_grid_limit)
+                       : host::launch_typed<64, false, false, false>(prm, st, g_grid_limit);
+    return a.out_f32 ? host::launch_typed<128, true, false, false>(prm, st, g_grid_limit)
+                     : host::launch_typed<128, false, false, false>(prm, st, g_grid_limit);
   }
-  if (a.d == 64) return a.out_f32 ? launch_typed<64, true>(prm, st) : launch_typed<64, false>(prm, st);
-  return a.out_f32 ? launch_typed<128, true>(prm, st) : launch_typed<128, false>(prm, st);
+  if (short_items) return host::launch_short(prm, a.d, a.out_f32, st, g_grid_limit);
+  if (a.d == 64)
+    return a.out_f32 ? host::launch_typed<64, true>(prm, st, g_grid_limit)
+                     : host::launch_typed<64, false>(prm, st, g_grid_limit);
+  return a.out_f32 ? host::launch_typed<128, true>(prm, st, g_grid_limit)
+                   : host::launch_typed<128, false>(prm, st, g_grid_limit);
 }
 
 void set_grid_limit(int max_ctas) { g_grid_limit = max_ctas > 0 ? max_ctas : 0; }

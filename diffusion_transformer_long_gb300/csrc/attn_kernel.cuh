@@ -26,6 +26,8 @@
 //   warp  9     TMEM allocator + single-thread issuer of S = Q K^T
 //   warp 10     single-thread issuer of O += P V       (warp 11 idle)
 //   warps 12-15 epilogue: O_t out of TMEM, normalised, stored; both Q tiles
+//               (kSoftDrain, for work items of few KV tiles: each softmax warpgroup drains
+//               its own O_t once the item's last PV has landed, and warps 12-15 idle)
 // Two issuers keep the tensor pipe fed: its queue is about one instruction deep,
 // and a barrier wait stalls the waiting thread for longer than one MMA, so while
 // one issuer waits the other issues.
@@ -97,13 +99,20 @@ constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;     // S = Q K^T issuer, owns the TMEM allocation
 constexpr int kPvWarp = 10;     // O += P V issuer
 constexpr int kEpiWarp0 = 12;   // warps 12-15: epilogue warpgroup
-// Register split (setmaxnreg): 512 threads launch with 128 registers each (65536);
-// softmax warpgroups grow to 176, the producer/issuer warpgroup shrinks to 72 and
-// the epilogue warpgroup to 88: 2*128*176 + 128*72 + 128*88 = 65536, and per SM
-// sub-partition (one warp of each warpgroup) 176+176+72+88 = 512.
-constexpr uint32_t kRegsSoftmax = 176;
-constexpr uint32_t kRegsIssue = 72;
-constexpr uint32_t kRegsEpilogue = 88;
+// Register split (setmaxnreg): 512 threads launch with 128 registers each (65536); the
+// producer/issuer warpgroup shrinks to 72 and the softmax warpgroups take what the
+// epilogue warpgroup leaves: per SM sub-partition (one warp of each warpgroup) the four
+// shares add up to 512, i.e. 65536 registers over the block.
+//   epilogue drains O:        softmax 176, issuers 72, epilogue 88
+//   softmax drains O (short
+//   items, kSoftDrain):       softmax 208, issuers 72, the idle epilogue warpgroup 24
+template <bool kSoftDrain>
+struct RegSplit {
+  static constexpr uint32_t kIssue = 72;
+  static constexpr uint32_t kEpilogue = kSoftDrain ? 24 : 88;
+  static constexpr uint32_t kSoftmax = (512 - kIssue - kEpilogue) / 2;
+  static_assert(kSoftmax % 8 == 0 && 2 * kSoftmax + kIssue + kEpilogue == 512, "register split");
+};
 constexpr float kRescaleLog2 = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 constexpr int kStatusTimeout = 1;
@@ -495,7 +504,98 @@ __device__ __forceinline__ void add_bf16x2(float& acc_lo, float& acc_hi, uint32_
       : "r"(w));
 }
 
-template <int D, bool kAccum, bool kLse>
+// One butterfly stage of a warp-wide register<->lane transpose: lane bit kLaneBit and bit
+// kRegBit of the register index trade meanings (each pair of registers differing in that
+// register bit exchanges one value with the lane differing in that lane bit).
+template <int kLaneBit, int kRegBit, int N>
+__device__ __forceinline__ void swap_lane_reg_bit(uint32_t (&x)[N], int lane) {
+  const bool hi = (lane >> kLaneBit) & 1;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (i & (1 << kRegBit)) continue;
+    const int j = i | (1 << kRegBit);
+    const uint32_t send = hi ? x[i] : x[j];
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1 << kLaneBit);
+    x[i] = hi ? recv : x[i];
+    x[j] = hi ? x[j] : recv;
+  }
+}
+
+// 32 bytes to global memory: one 32-byte store when dst is 32-byte aligned, else two 16-byte ones.
+__device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uint32_t* a) {
+  if (align32) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a[0]),
+                 "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a[0]), "r"(a[1]),
+                 "r"(a[2]), "r"(a[3])
+                 : "memory");
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(static_cast<char*>(dst) + 16),
+                 "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+                 : "memory");
+  }
+}
+
+// O_t of a finished work item out of tensor memory (the drain), run by the softmax warpgroup
+// that built it: every thread loads its row (all D columns: the scores' registers are free
+// at this point), the tensor-memory buffer is released to the next item's first PV at once,
+// then the row is normalised by 1 / lp and stored.  fp32 rows go through two butterfly
+// stages of warp shuffles (lane bits 4,3 <-> register bits 4,3 of each 32-column chunk), so
+// that one warp store covers 8 rows x 128 contiguous bytes rather than 32 rows x 32 bytes
+// (a quarter of the L1 wavefronts per byte, which keeps the stores from holding up the
+// other warpgroup's shared-memory P writes); bf16 rows are stored from the row-per-thread
+// layout.
+template <int D, bool kOutF32>
+__device__ __forceinline__ void drain_o(const AttnParams& p, uint32_t tO, uint32_t o_empty_bar,
+                                        const Item& item, int t, int quarter, int lane,
+                                        float inv_l) {
+  uint32_t o[D / 32][32];
+  ptx::tc_fence_after();
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
+  ptx::tmem_wait_ld();
+  ptx::tc_fence_before();
+  ptx::mbar_arrive(o_empty_bar);  // the next item's first PV may overwrite O_t
+  const size_t out_off = item.out_off(p);
+  const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
+  if constexpr (kOutF32) {
+    const int r_lo = lane & 7, cgrp = lane >> 3;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * inv_l);
+      swap_lane_reg_bit<4, 4>(o[c], lane);
+      swap_lane_reg_bit<3, 3>(o[c], lane);
+      // o[c][8*rr + i] = (row row0w + 8*rr + r_lo, column 32*c + 8*cgrp + i)
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int row_k = row0w + rr * 8 + r_lo;
+        if (row_k < p.n_q)
+          st_global_32B(p.out_f32 + out_off + static_cast<size_t>(row_k) * p.o_sn + c * 32 +
+                            cgrp * 8,
+                        p.out_align32, &o[c][rr * 8]);
+      }
+    }
+  } else {
+    const int row = row0w + lane;
+    if (row < p.n_q) {
+      __nv_bfloat16* dst = p.out_bf16 + out_off + static_cast<size_t>(row) * p.o_sn;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t wd[16];  // 32 columns of this thread's row as bf16 pairs
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          wd[i] = ptx::pack_bf16x2(__uint_as_float(o[c][2 * i]) * inv_l,
+                                   __uint_as_float(o[c][2 * i + 1]) * inv_l);
+        st_global_32B(dst + c * 32, p.out_align32, &wd[0]);
+        st_global_32B(dst + c * 32 + 16, p.out_align32, &wd[8]);
+      }
+    }
+  }
+}
+
+template <int D, bool kOutF32, bool kAccum, bool kLse, bool kSoftDrain>
 __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, uint32_t tmem,
                                            int t, int warp, int lane,
                                            volatile int* abort_flag) {
@@ -673,7 +773,18 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     const Item item = item_of(p, w);
     const int row = item.q_row0 + t * kBlockM + r;
     float* const lse_row = p.lse + item.lse_off(p) + row;
-    if constexpr (!kAccum) {
+    if constexpr (kSoftDrain) {
+      // Short items: this warpgroup drains its own O_t once the item's last PV has landed
+      // (drain_o), instead of handing it to the epilogue warpgroup.
+      if constexpr (kLse) {
+        if (row < p.n_q) *lse_row = lse2 * kLn2;
+      } else {
+        (void)lse_row;
+        (void)lse2;
+      }
+      if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+      drain_o<D, kOutF32>(p, tO, bar(L::bOEmpty + t), item, t, quarter, lane, 1.f / lp);
+    } else if constexpr (!kAccum) {
       // Slot [t][r] = 1 / lp, reused once the epilogue has taken the previous item's value.
       if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
       hand[t * kBlockM + r] = 1.f / lp;
@@ -700,39 +811,6 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     }
   }
   if (!ok) raise_abort(p, abort_flag);
-}
-
-// One butterfly stage of a warp-wide register<->lane transpose: lane bit kLaneBit and bit
-// kRegBit of the register index trade meanings (each pair of registers differing in that
-// register bit exchanges one value with the lane differing in that lane bit).
-template <int kLaneBit, int kRegBit, int N>
-__device__ __forceinline__ void swap_lane_reg_bit(uint32_t (&x)[N], int lane) {
-  const bool hi = (lane >> kLaneBit) & 1;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    if (i & (1 << kRegBit)) continue;
-    const int j = i | (1 << kRegBit);
-    const uint32_t send = hi ? x[i] : x[j];
-    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 1 << kLaneBit);
-    x[i] = hi ? recv : x[i];
-    x[j] = hi ? x[j] : recv;
-  }
-}
-
-// 32 bytes to global memory: one 32-byte store when dst is 32-byte aligned, else two 16-byte ones.
-__device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uint32_t* a) {
-  if (align32) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a[0]),
-                 "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
-                 : "memory");
-  } else {
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a[0]), "r"(a[1]),
-                 "r"(a[2]), "r"(a[3])
-                 : "memory");
-    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(static_cast<char*>(dst) + 16),
-                 "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
-                 : "memory");
-  }
 }
 
 // Epilogue warpgroup (warps 12-15): for each work item and Q tile t, waits for the
@@ -921,9 +999,12 @@ __device__ __forceinline__ void epilogue_wg(const AttnParams& p, uint32_t sbase,
 }  // namespace detail
 
 // kLse = false: no LSE output (p.lse unused) and no unrounded row sum; O is unchanged.
-template <int D, bool kOutF32, bool kAccum, bool kLse = true>
+// kSoftDrain: the softmax warpgroups drain O themselves (for work items of few KV tiles, where
+// an item's drain would otherwise wait for the epilogue warpgroup's turn at every item).
+template <int D, bool kOutF32, bool kAccum, bool kLse = true, bool kSoftDrain = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnParams p) {
   static_assert(kLse || !kAccum, "the running merge needs the LSE");
+  static_assert(!(kSoftDrain && kAccum), "the running merge runs in the epilogue warpgroup");
   using L = AttnSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -971,11 +1052,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::kTmemSlot);
   if (threadIdx.x == 0) DIT_TRACE(kTrCta, 0);
 
+  using Regs = RegSplit<kSoftDrain>;
   if (warp < kLoadWarp) {
-    ptx::setmaxnreg_inc<kRegsSoftmax>();
-    detail::softmax_wg<D, kAccum, kLse>(p, sbase, tmem, warp >> 2, warp, lane, abort_flag);
+    ptx::setmaxnreg_inc<Regs::kSoftmax>();
+    detail::softmax_wg<D, kOutF32, kAccum, kLse, kSoftDrain>(p, sbase, tmem, warp >> 2, warp, lane,
+                                                              abort_flag);
   } else if (warp < kEpiWarp0) {
-    ptx::setmaxnreg_dec<kRegsIssue>();
+    ptx::setmaxnreg_dec<Regs::kIssue>();
     if (warp == kLoadWarp) {
       if (lane == 0) detail::producer<D>(p, sbase, abort_flag);
     } else if (warp == kMmaWarp) {
@@ -985,8 +1068,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     __syncwarp();
   } else {
-    ptx::setmaxnreg_dec<kRegsEpilogue>();
-    detail::epilogue_wg<D, kOutF32, kAccum>(p, sbase, tmem, warp, lane, abort_flag);
+    ptx::setmaxnreg_dec<Regs::kEpilogue>();
+    if constexpr (!kSoftDrain)
+      detail::epilogue_wg<D, kOutF32, kAccum>(p, sbase, tmem, warp, lane, abort_flag);
   }
 
   ptx::tc_fence_before();

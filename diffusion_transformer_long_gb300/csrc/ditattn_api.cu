@@ -199,6 +199,32 @@ dit_status validate_splits(int splits, int n_kv, const void* workspace, size_t w
   return DIT_OK;
 }
 
+// Chunk arguments (all virtual ranks in one launch): the attention arguments for the
+// partial blocks, 1 <= p <= 64 increasing chunk starts within [0, n_kv], and p partial blocks
+// and LSE rows clear of the inputs and of each other.
+dit_status validate_chunks(const void* q, const void* k, const void* v, void* partials,
+                           float* lses, int B, int H, int N_q, int n_kv, int D,
+                           long long kv_head_stride, int p, const int* chunk_starts, float scale,
+                           dit_dtype partial_dtype) {
+  dit_status s = validate_attention(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride,
+                                    scale, partial_dtype);
+  if (s != DIT_OK) return s;
+  if (p < 1 || p > 64 || !chunk_starts) return DIT_ERR_INVALID_ARG;
+  if (chunk_starts[0] < 0 || chunk_starts[p] > n_kv) return DIT_ERR_INVALID_ARG;
+  for (int c = 0; c < p; ++c)
+    if (chunk_starts[c + 1] <= chunk_starts[c]) return DIT_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  if (((static_cast<long long>(N_q) + 255) / 256) * bh * p > INT_MAX) return DIT_ERR_INVALID_ARG;
+  const long long rows = bh * N_q;
+  const Range rp = span(partials, p * rows * D * dtype_bytes(partial_dtype));
+  const Range rl = span(lses, p * rows * 4);
+  const long long kv_bytes = ((bh - 1) * kv_head_stride + static_cast<long long>(n_kv) * D) * 2;
+  for (Range in : {span(q, rows * D * 2), span(k, kv_bytes), span(v, kv_bytes)})
+    if (overlap(rp, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
+  if (overlap(rp, rl)) return DIT_ERR_INVALID_ARG;
+  return DIT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -227,22 +253,9 @@ dit_status dit_attn_chunks_fwd(const void* q, const void* k, const void* v, void
                                float* lses, int B, int H, int N_q, int n_kv, int D,
                                long long kv_head_stride, int p, const int* chunk_starts,
                                float scale, dit_dtype partial_dtype, dit_stream stream) {
-  dit_status s = validate_attention(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride,
-                                    scale, partial_dtype);
+  dit_status s = validate_chunks(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride, p,
+                                 chunk_starts, scale, partial_dtype);
   if (s != DIT_OK) return s;
-  if (p < 1 || p > 64 || !chunk_starts) return DIT_ERR_INVALID_ARG;
-  if (chunk_starts[0] < 0 || chunk_starts[p] > n_kv) return DIT_ERR_INVALID_ARG;
-  for (int c = 0; c < p; ++c)
-    if (chunk_starts[c + 1] <= chunk_starts[c]) return DIT_ERR_INVALID_ARG;
-  // All p partial blocks and LSE rows must stay clear of the inputs and of each other.
-  const long long bh = static_cast<long long>(B) * H;
-  const long long rows = bh * N_q;
-  const Range rp = span(partials, p * rows * D * dtype_bytes(partial_dtype));
-  const Range rl = span(lses, p * rows * 4);
-  const long long kv_bytes = ((bh - 1) * kv_head_stride + static_cast<long long>(n_kv) * D) * 2;
-  for (Range in : {span(q, rows * D * 2), span(k, kv_bytes), span(v, kv_bytes)})
-    if (overlap(rp, in) || overlap(rl, in)) return DIT_ERR_INVALID_ARG;
-  if (overlap(rp, rl)) return DIT_ERR_INVALID_ARG;
   return run_contiguous(q, k, v, partials, lses, B, H, N_q, n_kv, D, kv_head_stride, scale,
                         partial_dtype, stream, false, 1, nullptr, p, chunk_starts);
 }

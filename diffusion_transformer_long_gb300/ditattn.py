@@ -131,6 +131,35 @@ def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check_out(out, lse, shape, device, out_name="out", lse_name="lse", contiguous=True):
+    """Caller-provided outputs: `out` a [shape] fp32 or bf16 tensor and `lse` a contiguous fp32
+    [shape[:-1]] tensor, both on `device` (the C ABI cannot see buffer sizes, so a wrong shape,
+    dtype, layout or device must be stopped here).  `contiguous=False` lets `out` be any view
+    whose last dimension is contiguous (the strided entry point checks the strides itself)."""
+    shape = tuple(int(x) for x in shape)
+    if out is not None:
+        if not isinstance(out, torch.Tensor) or out.device != device:
+            raise ValueError(f"{out_name} must be a tensor on {device}")
+        if tuple(out.shape) != shape:
+            raise ValueError(f"{out_name} must have shape {list(shape)}, got {list(out.shape)}")
+        if out.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError(f"{out_name} must be float32 or bfloat16, got {out.dtype}")
+        if contiguous and not out.is_contiguous():
+            raise ValueError(f"{out_name} must be contiguous")
+        if not contiguous and out.stride(-1) != 1:
+            raise ValueError(f"{out_name} must have a contiguous last dimension")
+    if lse is not None:
+        if not isinstance(lse, torch.Tensor) or lse.device != device:
+            raise ValueError(f"{lse_name} must be a tensor on {device}")
+        if tuple(lse.shape) != shape[:-1]:
+            raise ValueError(f"{lse_name} must have shape {list(shape[:-1])}, "
+                             f"got {list(lse.shape)}")
+        if lse.dtype != torch.float32:
+            raise ValueError(f"{lse_name} must be float32, got {lse.dtype}")
+        if not lse.is_contiguous():
+            raise ValueError(f"{lse_name} must be contiguous")
+
+
 def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, stream=None,
              with_lse=True):
     """Fused attention over all keys.  q, k, v: CUDA bf16 [B, H, N, D] contiguous.
@@ -143,6 +172,7 @@ def attn_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.float32, s
         raise ValueError("k and v must be contiguous with q's shape")
     B, H, N, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_out(out, lse, (B, H, N, D), q.device)
     if out is None:
         out = torch.empty((B, H, N, D), device=q.device, dtype=out_dtype)
     if lse is None and with_lse:
@@ -178,8 +208,7 @@ def attn_fwd_strided(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.fl
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     if out is None:
         out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
-    if tuple(out.shape) != (B, H, Nq, D):
-        raise ValueError("out must be a [B, H, N_q, D] view")
+    _check_out(out, lse, (B, H, Nq, D), q.device, contiguous=False)
     if lse is None:
         lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
     qs, ks, vs, os_ = (view_strides(t) for t in (q, k, v, out))
@@ -285,6 +314,7 @@ def attn_chunk_fwd_splitkv(q, k, v, out=None, lse=None, scale=None, out_dtype=to
         raise ValueError("k and v chunks must have the same head stride")
     n_kv = k.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_out(out, lse, (B, H, Nq, D), q.device)
     if out is None:
         out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
     if lse is None:
@@ -314,6 +344,9 @@ def attn_chunk_fwd_splitkv_noalloc(q, k, v, out, lse, scale=None, splits=None, s
         raise ValueError("k and v chunks must have the same head stride")
     n_kv = k.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    if out is None or lse is None:
+        raise ValueError("out and lse are required: this path allocates nothing")
+    _check_out(out, lse, (B, H, Nq, D), q.device)
     with torch.cuda.device(q.device):
         if splits is None:
             splits = int(lib().dit_attn_splitkv_suggest(B, H, Nq, n_kv))
@@ -342,6 +375,7 @@ def stale_kv_attention(q, k_new, v_new, k_buf, v_buf, row0, out=None, lse=None, 
             or tuple(k_buf.shape[:2]) != (B, H) or k_buf.shape[3] != D:
         raise ValueError("shape mismatch between the patch and the KV buffers")
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_out(out, lse, (B, H, m, D), q.device)
     if out is None:
         out = torch.empty((B, H, m, D), device=q.device, dtype=out_dtype)
     if lse is None:
@@ -389,6 +423,7 @@ def attn_chunk_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.floa
         raise ValueError("k and v chunks must have the same head stride")
     n_kv = k.shape[2]
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_out(out, lse, (B, H, Nq, D), q.device)
     if out is None:
         out = torch.empty((B, H, Nq, D), device=q.device, dtype=out_dtype)
     if lse is None:
@@ -402,11 +437,9 @@ def attn_chunk_fwd(q, k, v, out=None, lse=None, scale=None, out_dtype=torch.floa
     return out, lse
 
 
-def attn_chunks_fwd(q, k, v, chunks, partials=None, lses=None, scale=None,
-                    partial_dtype=torch.float32, stream=None):
-    """Every chunk's partial (O_c, lse_c) of the ring decomposition in one launch
-    (dit_attn_chunks_fwd): chunk c is keys [s_c, s_c + chunks[c]) of k / v, s_c the sum of the
-    earlier lengths.  Returns (partials [p, B, H, N_q, D] of partial_dtype, lses [p, B, H, N_q])."""
+def _chunk_plan(q, k, v, chunks, partials, lses, partial_dtype):
+    """Shared argument handling of the all-chunks-in-one-launch calls: (hs, starts, partials,
+    lses) with the host chunk-start table and the partial buffers (allocated unless given)."""
     _check_qkv(q, k, v)
     B, H, Nq, D = q.shape
     if k.shape != v.shape or k.shape[0] != B or k.shape[1] != H or k.shape[3] != D:
@@ -423,13 +456,23 @@ def attn_chunks_fwd(q, k, v, chunks, partials=None, lses=None, scale=None,
         starts[c] = acc
         acc += int(n)
     starts[p] = acc
-    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    _check_out(partials, lses, (p, B, H, Nq, D), q.device, "partials", "lses")
     if partials is None:
         partials = torch.empty((p, B, H, Nq, D), device=q.device, dtype=partial_dtype)
     if lses is None:
         lses = torch.empty((p, B, H, Nq), device=q.device, dtype=torch.float32)
-    if not partials.is_contiguous() or not lses.is_contiguous():
-        raise ValueError("partials and lses must be contiguous")
+    return hs, starts, partials, lses
+
+
+def attn_chunks_fwd(q, k, v, chunks, partials=None, lses=None, scale=None,
+                    partial_dtype=torch.float32, stream=None):
+    """Every chunk's partial (O_c, lse_c) of the ring decomposition in one launch
+    (dit_attn_chunks_fwd): chunk c is keys [s_c, s_c + chunks[c]) of k / v, s_c the sum of the
+    earlier lengths.  Returns (partials [p, B, H, N_q, D] of partial_dtype, lses [p, B, H, N_q])."""
+    hs, starts, partials, lses = _chunk_plan(q, k, v, chunks, partials, lses, partial_dtype)
+    B, H, Nq, D = q.shape
+    p = len(chunks)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     with torch.cuda.device(q.device):
         st = lib().dit_attn_chunks_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(partials), _ptr(lses), B, H,
                                        Nq, k.shape[2], D, hs, p, starts, scale, _dt(partials.dtype),
@@ -475,6 +518,7 @@ def attn_lse_merge(partials, lses, out=None, lse=None, out_dtype=torch.float32, 
             or not lses.is_contiguous():
         raise ValueError("lses must be contiguous fp32 [p, B, H, N]")
     p, B, H, N, D = partials.shape
+    _check_out(out, lse, (B, H, N, D), partials.device)
     if out is None:
         out = torch.empty((B, H, N, D), device=partials.device, dtype=out_dtype)
     if lse is None:
@@ -512,7 +556,8 @@ def chunk_attention(q, k, v, chunks, scale=None, out_dtype=torch.float32,
                     batched=False):
     """Ring decomposition on one GPU: one dit_attn_chunk_fwd per KV chunk (virtual rank), or
     with batched=True all chunks in one dit_attn_chunks_fwd launch (bitwise the same partials),
-    then one dit_attn_lse_merge.  `chunks` lists the chunk lengths (sum = N_kv)."""
+    then one dit_attn_lse_merge.  `chunks` lists the chunk lengths (sum = N_kv).  Returns
+    (out, lse)."""
     B, H, Nq, D = q.shape
     if sum(chunks) != k.shape[2]:
         raise ValueError("chunk lengths must sum to the number of keys")

@@ -15,9 +15,16 @@
  *    bf16 (IEEE binary16-brain, 2 bytes).  LSE buffers are fp32 [B, H, N].
  *  - lse is the NATURAL log of sum_j exp(scale * q_i . k_j) over the keys the
  *    call covers (the kernels work in base 2 internally and convert).
- *  - The caller owns every buffer.  The library allocates no device memory;
- *    it keeps only a cache of host-side TMA-descriptor encoders and one
- *    device status word.
+ *  - The caller owns every buffer.  The library calls no device allocator.
+ *    Besides a cache of host-side TMA-descriptor encoders it holds two
+ *    fixed device arrays in its own module: one status word, and the 128 MiB
+ *    scratch array of dit_attn_chunk_fwd_splitkv_noalloc.  The CUDA runtime
+ *    reserves them on a device when it loads the library's device code there:
+ *    on the first call that uses that device under the default lazy module
+ *    loading, or when the library is loaded under CUDA_MODULE_LOADING=EAGER.
+ *    On a device too full to take them, that first call fails with
+ *    DIT_ERR_CUDA.  Device addresses are looked up once per device number and
+ *    assume the runtime's primary context (no cudaDeviceReset in between).
  *  - Calls are asynchronous on `stream` (0 = legacy default stream).  Argument
  *    errors are returned before anything is launched.  A launch failure
  *    returns DIT_ERR_CUDA.  Device-side timeouts (a bounded wait that

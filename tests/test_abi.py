@@ -317,3 +317,55 @@ def test_kv_head_stride_of_views():
     assert da.kv_head_stride(torch.zeros(4, 1, 9, 64)[:, :, 2:5]) == 9 * 64
     with pytest.raises(ValueError):
         da.kv_head_stride(full.transpose(2, 3))
+
+
+def noalloc(lib, n_kv=1000, splits=3, out=OUT, lse=LSE, q=Q, B=1, H=2, N=256, D=128):
+    return lib.dit_attn_chunk_fwd_splitkv_noalloc(q, K, V, out, lse, B, H, N, n_kv, D, N * D * 8,
+                                                  0.088, 0, splits, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(splits=0), da.DIT_ERR_INVALID_ARG),
+    (dict(splits=65, n_kv=65 * 128), da.DIT_ERR_INVALID_ARG),      # more than 64 splits
+    (dict(splits=9, n_kv=1000), da.DIT_ERR_INVALID_ARG),           # more splits than key tiles
+    (dict(lse=None), da.DIT_ERR_INVALID_ARG),
+    (dict(out=None), da.DIT_ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p((1 << 40) + 4096)), da.DIT_ERR_INVALID_ARG),   # out inside q
+    (dict(lse=ctypes.c_void_p((4 << 40) + 1024)), da.DIT_ERR_INVALID_ARG),   # lse inside out
+    (dict(D=96), da.DIT_ERR_UNSUPPORTED),
+    # partials of 24 heads x 27280 rows x 8 splits exceed the 128 MiB scratch
+    (dict(B=1, H=24, N=27280, n_kv=27280 * 8, splits=8), da.DIT_ERR_UNSUPPORTED),
+])
+def test_noalloc_splitkv_validation(lib, kw, status):
+    assert noalloc(lib, **kw) == status
+
+
+CPU = torch.device("cpu")
+
+
+@pytest.mark.parametrize("bad", [
+    dict(out=torch.zeros(1, 2, 8, 32)),                                 # wrong shape
+    dict(out=torch.zeros(1, 2, 8, 64, dtype=torch.float16)),            # wrong dtype
+    dict(out=torch.zeros(1, 2, 64, 8).transpose(2, 3)),                 # not contiguous
+    dict(lse=torch.zeros(1, 2, 8, dtype=torch.bfloat16)),               # lse not fp32
+    dict(lse=torch.zeros(1, 2, 9)),                                     # lse wrong shape
+    dict(lse=torch.zeros(1, 2, 16)[:, :, ::2]),                         # lse not contiguous
+    dict(out=[0.0] * 4),                                                # not a tensor
+])
+def test_binding_rejects_bad_caller_outputs(bad):
+    kw = dict(out=None, lse=None)
+    kw.update(bad)
+    with pytest.raises(ValueError):
+        da._check_out(kw["out"], kw["lse"], (1, 2, 8, 64), CPU)
+
+
+def test_binding_output_checks_accept_good_outputs_and_views():
+    da._check_out(torch.zeros(1, 2, 8, 64), torch.zeros(1, 2, 8), (1, 2, 8, 64), CPU)
+    da._check_out(torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16), None, (1, 2, 8, 64), CPU)
+    # a token-major view is fine where the entry point takes strides
+    bsnd = torch.zeros(1, 8, 2, 64).transpose(1, 2)
+    da._check_out(bsnd, None, (1, 2, 8, 64), CPU, contiguous=False)
+    with pytest.raises(ValueError):
+        da._check_out(bsnd, None, (1, 2, 8, 64), CPU)
+    with pytest.raises(ValueError):          # a tensor on another device
+        da._check_out(torch.zeros(1, 2, 8, 64), None, (1, 2, 8, 64), torch.device("cuda", 0))
