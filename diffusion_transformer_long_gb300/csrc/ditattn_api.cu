@@ -409,15 +409,34 @@ int dit_attn_splitkv_suggest(int B, int H, int N_q, int n_kv) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
     return 1;
-  // Persistent grid: one CTA per SM walks the (head, Q pair) items.  Below about four waves
-  // the last partial wave idles a large share of the SMs; split the keys of every item so
-  // that there are about six waves, keeping at least 8 KV tiles per split.
+  // Estimated time of each split count S on the persistent grid (one CTA per SM walking the
+  // (head, Q pair, key range) items): ceil(items * S / SMs) waves, each as long as one item's
+  // ceil(T / S) KV tiles plus a fixed per-item cost (Q load, first and last tiles, the O drain:
+  // about four tile periods, measured), plus for S > 1 the merge launch, which reads the S fp32
+  // partials and writes the output at HBM speed.  A tile period is about 1.5 us (both Q tiles of
+  // a CTA against one 128-key tile).  The cheapest S wins (ties: fewer splits).
+  constexpr double kTileUs = 1.5, kItemTiles = 4.0, kMergeLaunchUs = 5.0, kHbmBytesPerUs = 6.5e6;
   const long long items = static_cast<long long>(B) * H * ((N_q + 255) / 256);
-  if (items >= 4LL * sms) return 1;
   const long long tiles = (n_kv + 127) / 128;
-  long long s = (6LL * sms + items - 1) / items;
-  s = std::min<long long>(s, std::min<long long>(16, tiles / 8));
-  return s < 2 ? 1 : static_cast<int>(s);
+  const double rows = static_cast<double>(B) * H * N_q;
+  auto cost = [&](long long S) {
+    const long long waves = (items * S + sms - 1) / sms;
+    const long long item_tiles = (tiles + S - 1) / S;
+    double us = static_cast<double>(waves) * (static_cast<double>(item_tiles) + kItemTiles) * kTileUs;
+    if (S > 1) us += kMergeLaunchUs + rows * (S + 1) * (128 * 4 + 4) / kHbmBytesPerUs;
+    return us;
+  };
+  long long best = 1;
+  double best_us = cost(1);
+  const long long s_max = std::min<long long>(16, tiles / 2);
+  for (long long S = 2; S <= s_max; ++S) {
+    const double us = cost(S);
+    if (us < best_us) {
+      best_us = us;
+      best = S;
+    }
+  }
+  return static_cast<int>(best);
 }
 
 dit_status dit_attn_chunk_fwd_splitkv(const void* q, const void* k, const void* v, void* out,

@@ -220,10 +220,12 @@ dit_status dit_attn_chunk_fwd_splitkv_noalloc(const void* q, const void* k, cons
  * size is not positive): splits * B*H*N_q * (D + 1) * 4, the LSE part 256-byte aligned. */
 size_t dit_attn_splitkv_workspace_bytes(int B, int H, int N_q, int D, int splits);
 
-/* A split count for an N_q x n_kv problem on the current device: 1 when the
- * persistent grid already gets at least four waves of (head, Q pair) items, else
- * enough splits for about six waves, keeping at least 8 key tiles per split (at
- * most 16).  Reads the device's SM count; returns 1 if it cannot. */
+/* A split count for an N_q x n_kv problem on the current device (1 to 16, at least two
+ * key tiles per split): the one with the smallest estimated time, where the estimate is the
+ * persistent grid's waves of (head, Q pair, key range) items times one item's KV tiles plus
+ * a fixed per-item cost, plus (for splits > 1) the merge launch and its fp32 partial
+ * traffic.  Never suggests a split the estimate puts behind no split.  Reads the device's SM
+ * count; returns 1 if it cannot. */
 int dit_attn_splitkv_suggest(int B, int H, int N_q, int n_kv);
 
 /*

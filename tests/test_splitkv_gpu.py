@@ -111,3 +111,20 @@ def test_stale_kv_with_splits():
     da.check()
     assert torch.equal(kb.cpu(), k_ref) and torch.equal(vb.cpu(), v_ref)
     check(o, lse, o_ref, lse_ref, "stale-KV, suggested splits")
+
+
+def test_split_suggestion_follows_the_cost_estimate():
+    """The suggestion keeps patches whose items already fill the grid unsplit (FLUX, CFG and
+    Wan2.1 patch shapes, where splitting measured slower), and splits a Wan2.2 patch (336
+    items of 214 tiles: 3 waves unsplit) into 3 or 4 ranges."""
+    L = da.lib()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with torch.cuda.device(0):
+        assert L.dit_attn_splitkv_suggest(1, 24, 1152, 4608) == 1     # FLUX patch
+        assert L.dit_attn_splitkv_suggest(2, 24, 1536, 4608) == 1     # CFG patch
+        assert L.dit_attn_splitkv_suggest(1, 40, 9450, 75600) == 1    # Wan2.1 patch
+        s = L.dit_attn_splitkv_suggest(1, 24, 3410, 27280)            # Wan2.2 patch
+        if sms == 152:
+            assert s in (3, 4)
+        assert 1 <= s <= 16
+        assert L.dit_attn_splitkv_suggest(1, 1, 64, 128) == 1         # one key tile: no split
