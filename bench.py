@@ -834,6 +834,8 @@ def run_profile_case(args):
             da.attn_lse_merge(parts, lses, out=out, lse=lse)
         elif args.profile_case == "transpose":
             da.bsnd_to_bhnd(src, out=dst)
+        elif args.profile_case == "cross":
+            da.attn_chunk_fwd(q, k[:, :, :512], v[:, :, :512], out=out, lse=lse, scale=w.scale)
     torch.cuda.synchronize(dev)
     da.check(dev)
     return 0
@@ -852,7 +854,7 @@ def main(argv=None):
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload record (every config's fused and chunk paths)")
     ap.add_argument("--profile-case", choices=["fused", "chunks", "chunk", "accumulate", "merge",
-                                               "transpose"],
+                                               "transpose", "cross"],
                     help="run only this path, untimed (for ncu captures); prints nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3:

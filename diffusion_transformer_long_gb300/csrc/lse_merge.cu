@@ -8,8 +8,7 @@
 // D*sizeof(out) + 4 bytes per query row.  Each thread owns one 16-byte vector
 // of one row (4 fp32 or 8 bf16 partial elements); the threads of a row are
 // consecutive, so every partial row is read by fully coalesced 16-byte
-// streaming loads.  The per-row arithmetic (merge_math.cuh) is the one the
-// attention kernel's merged-chunks form uses, bit for bit.
+// streaming loads.  The per-row arithmetic is in merge_math.cuh.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

@@ -198,6 +198,28 @@ def test_query_and_key_counts_differ():
     assert_parity(o, lse, o_ref, lse_ref, "N_q=1300, n_kv=512")
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_cross_attention_512_keys_full_shape(out_dtype):
+    """The short-KV shape at full size, in the launch bench.py times: all 27280 Wan2.2 queries
+    of 24 heads against the first 512 rows of K and V (views with the full buffer's head
+    stride).  Items have 4 key tiles, so this is the short-item (soft-drain) form; sampled
+    rows (all heads, first/last 16 included) against the oracle."""
+    w = synth.WORKLOADS["wan22"]
+    q, k, v = synth.make_qkv(w)
+    n_txt = 512
+    rows = synth.sample_rows(w.N, 256, seed=w.seed + 1)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, kv_start=0, kv_len=n_txt, rows=rows)
+    qd, kd, vd = to_dev(q, k, v)
+    del q, k, v
+    o, lse = da.attn_chunk_fwd(qd, kd[:, :, :n_txt], vd[:, :, :n_txt], scale=w.scale,
+                               out_dtype=out_dtype)
+    da.check()
+    assert o.dtype == out_dtype and o.shape == qd.shape
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, f"cross 27280x512 {out_dtype}",
+                  bf16_out=out_dtype == torch.bfloat16)
+
+
 # ----------------------------------------------------------------- closed forms / invariants
 @pytest.fixture(scope="module")
 def flux_inputs():
@@ -376,6 +398,45 @@ def test_persistent_grid_many_items_per_cta(limit):
             assert_parity(orr, lrr, o_ref, lse_ref, f"grid={limit} D={D} ring accumulate")
     finally:
         da.set_grid_limit(0)
+
+
+def outlier_qkv(B, H, N, D, seed):
+    """CFG-stress-like inputs (the cfg workload's recipe at another shape): Q, K x gain and a
+    fraction of keys x outlier gain, so the running max keeps rising and O is rescaled on most
+    tiles."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, N, D, generator=g) * synth.CFG_QK_GAIN
+    k = torch.randn(B, H, N, D, generator=g) * synth.CFG_QK_GAIN
+    v = torch.randn(B, H, N, D, generator=g)
+    n_out = int(synth.CFG_OUTLIER_FRACTION * N)
+    for b in range(B):
+        for h in range(H):
+            idx = torch.randperm(N, generator=g)[:n_out]
+            k[b, h, idx] *= synth.CFG_OUTLIER_GAIN
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("limit", [0, 1, 3])
+def test_rescale_on_capped_grid(limit):
+    """Inputs whose running max keeps rising, so O is rescaled (and P published whole) on
+    most tiles: items of more than 16 key tiles (fused, and all chunks in one launch), with
+    every CTA walking many items when the grid is capped."""
+    B, H, N, D = 2, 3, 2500, 128
+    q, k, v = outlier_qkv(B, H, N, D, seed=31)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    da.set_grid_limit(limit)
+    try:
+        o, lse = da.attn_fwd(qd, kd, vd, scale=scale)
+        ob, lb = da.attn_fwd(qd, kd, vd, scale=scale, out_dtype=torch.bfloat16)
+        oc, lc = da.chunk_attention(qd, kd, vd, (2100, 400), scale=scale)
+        da.check()
+    finally:
+        da.set_grid_limit(0)
+    assert_parity(o, lse, o_ref, lse_ref, f"grid={limit} outliers fused")
+    assert_parity(ob, lb, o_ref, lse_ref, f"grid={limit} outliers bf16", bf16_out=True)
+    assert_parity(oc, lc, o_ref, lse_ref, f"grid={limit} outliers chunks")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
