@@ -55,6 +55,32 @@ bool encode_view(CUtensorMap* m, const void* base, int d, int rows, int heads, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D map (d, rows, heads, batch, key range) of the output (bf16 or fp32) of a short-item
+// pass, for its TMA stores: boxes of 128 rows x 128 bytes (64 bf16 or 32 fp32 columns),
+// 128-byte swizzle (the P tile's layout); rows past `rows` are not written.  Range r's
+// output starts range_stride elements after range r-1's (one range: the stride only has to
+// be valid).
+bool encode_out_view(CUtensorMap* m, void* base, bool f32, int d, int rows, int heads, int batch,
+                     int ranges, const Strides& st, long long range_stride) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  const cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(batch),
+                              static_cast<cuuint64_t>(ranges)};
+  const cuuint64_t strides[4] = {static_cast<cuuint64_t>(st.n_) * es,
+                                 static_cast<cuuint64_t>(st.h_) * es,
+                                 static_cast<cuuint64_t>(st.b_) * es,
+                                 static_cast<cuuint64_t>(range_stride) * es};
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(kBlockM),
+                             1, 1, 1};
+  const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base,
+            dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
@@ -115,14 +141,19 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
   } else if (split) {
     item_tiles = (prm.tiles_total + a.splits - 1) / a.splits;
   }
-  const bool short_items = item_tiles <= host::kShortItemTiles;
+  // Short items store O (or part of it) through a TMA map of the output; where the output
+  // view cannot be mapped (alignment), they take the epilogue-drain form instead.
+  bool short_items = item_tiles <= host::kShortItemTiles && !a.accumulate;
+  if (short_items)
+    short_items = encode_out_view(&prm.tm_o, obase, f32, a.d, a.n_q, a.heads, a.batch, prm.splits,
+                                  os, (split || batched) ? prm.ws_o_stride : os.b_ * a.batch);
   if (a.accumulate) {
     if (!a.out_f32) return cudaErrorInvalidValue;
     return a.d == 64 ? host::launch_typed<64, true, true>(prm, st, g_grid_limit)
                      : host::launch_typed<128, true, true>(prm, st, g_grid_limit);
   }
   if (split) {
-    const cudaError_t e = short_items ? host::launch_short(prm, a.d, true, st, g_grid_limit)
+    const cudaError_t e = short_items ? host::launch_short(prm, a.d, true, true, st, g_grid_limit)
                           : a.d == 64 ? host::launch_typed<64, true>(prm, st, g_grid_limit)
                                       : host::launch_typed<128, true>(prm, st, g_grid_limit);
     if (e != cudaSuccess) return e;
@@ -139,13 +170,14 @@ cudaError_t launch_attention(const AttnLaunch& a, cudaStream_t st) {
     return launch_merge(m, st);
   }
   if (!a.lse) {  // no LSE output (one key range; checked above)
+    if (short_items) return host::launch_short(prm, a.d, a.out_f32, false, st, g_grid_limit);
     if (a.d == 64)
       return a.out_f32 ? host::launch_typed<64, true, false, false>(prm, st, g_grid_limit)
                        : host::launch_typed<64, false, false, false>(prm, st, g_grid_limit);
     return a.out_f32 ? host::launch_typed<128, true, false, false>(prm, st, g_grid_limit)
                      : host::launch_typed<128, false, false, false>(prm, st, g_grid_limit);
   }
-  if (short_items) return host::launch_short(prm, a.d, a.out_f32, st, g_grid_limit);
+  if (short_items) return host::launch_short(prm, a.d, a.out_f32, true, st, g_grid_limit);
   if (a.d == 64)
     return a.out_f32 ? host::launch_typed<64, true>(prm, st, g_grid_limit)
                      : host::launch_typed<64, false>(prm, st, g_grid_limit);

@@ -9,13 +9,19 @@
 namespace ditattn {
 namespace host {
 
-cudaError_t launch_short(const AttnParams& prm, int d, bool out_f32, cudaStream_t st,
+template <int D, bool kLse>
+cudaError_t launch_short_d(const AttnParams& prm, bool out_f32, cudaStream_t st, int grid_limit) {
+  return out_f32 ? launch_typed<D, true, false, kLse, true>(prm, st, grid_limit)
+                 : launch_typed<D, false, false, kLse, true>(prm, st, grid_limit);
+}
+
+cudaError_t launch_short(const AttnParams& prm, int d, bool out_f32, bool lse, cudaStream_t st,
                          int grid_limit) {
   if (d == 64)
-    return out_f32 ? launch_typed<64, true, false, true, true>(prm, st, grid_limit)
-                   : launch_typed<64, false, false, true, true>(prm, st, grid_limit);
-  return out_f32 ? launch_typed<128, true, false, true, true>(prm, st, grid_limit)
-                 : launch_typed<128, false, false, true, true>(prm, st, grid_limit);
+    return lse ? launch_short_d<64, true>(prm, out_f32, st, grid_limit)
+               : launch_short_d<64, false>(prm, out_f32, st, grid_limit);
+  return lse ? launch_short_d<128, true>(prm, out_f32, st, grid_limit)
+             : launch_short_d<128, false>(prm, out_f32, st, grid_limit);
 }
 
 }  // namespace host

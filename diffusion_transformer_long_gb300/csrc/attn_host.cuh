@@ -58,8 +58,9 @@ cudaError_t launch_typed(const AttnParams& prm, cudaStream_t st, int grid_limit)
 
 // Work items of at most this many KV tiles take the soft-drain form (attn_fwd_short.cu).
 constexpr int kShortItemTiles = 16;
-// The soft-drain instantiations (attn_fwd_short.cu): fused/chunk/split passes with the LSE.
-cudaError_t launch_short(const AttnParams& prm, int d, bool out_f32, cudaStream_t st,
+// The soft-drain instantiations (attn_fwd_short.cu): fused/chunk/split passes, with or
+// without the LSE; bf16 output needs prm.tm_o (the output's TMA map).
+cudaError_t launch_short(const AttnParams& prm, int d, bool out_f32, bool lse, cudaStream_t st,
                          int grid_limit);
 
 }  // namespace host

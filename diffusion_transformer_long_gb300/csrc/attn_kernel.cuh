@@ -122,6 +122,8 @@ struct AttnParams {
   CUtensorMap tm_q;   // (D, n_q, bh) bf16, box (64, 128, 1), 128B swizzle
   CUtensorMap tm_k;   // (D, n_kv, bh), head stride = kv_head_stride
   CUtensorMap tm_v;
+  CUtensorMap tm_o;   // output of the short-item form: (D, n_q, H, B, key range), boxes of
+                      // 128 rows x 128 bytes, 128B swizzle (the P tile's layout)
   float* out_f32;     // (fp32 output) or null; O[b][h][n][d] at b*o_sb + h*o_sh + n*o_sn + d
   __nv_bfloat16* out_bf16;  // (bf16 output) or null; same addressing
   long long o_sb, o_sh, o_sn;  // output strides in elements
@@ -172,7 +174,9 @@ struct AttnSmem {
   static constexpr int bOEmpty = bPVDone + 2;        // + tile: O_t read by the epilogue (128 arrivals)
   static constexpr int bEpiReady = bOEmpty + 2;      // + tile: normaliser of an item written (128)
   static constexpr int bEpiTaken = bEpiReady + 2;    // + tile: normaliser read by the epilogue (128)
-  static constexpr int bDrainS = bEpiTaken + 2;      // abort drain, S issuer
+  static constexpr int bStaged = bEpiTaken + 2;      // + tile: O_t staged in P_t (128 arrivals)
+  static constexpr int bStageFree = bStaged + 2;     // + tile: P_t's staged O read by the TMA
+  static constexpr int bDrainS = bStageFree + 2;     // abort drain, S issuer
   static constexpr int bDrainPV = bDrainS + 1;       // abort drain, PV issuer
   static constexpr int kNumBars = bDrainPV + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8;
@@ -537,19 +541,28 @@ __device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uin
   }
 }
 
-// O_t of a finished work item out of tensor memory (the drain), run by the softmax warpgroup
-// that built it: every thread loads its row (all D columns: the scores' registers are free
-// at this point), the tensor-memory buffer is released to the next item's first PV at once,
-// then the row is normalised by 1 / lp and stored.  fp32 rows go through two butterfly
-// stages of warp shuffles (lane bits 4,3 <-> register bits 4,3 of each 32-column chunk), so
-// that one warp store covers 8 rows x 128 contiguous bytes rather than 32 rows x 32 bytes
-// (a quarter of the L1 wavefronts per byte, which keeps the stores from holding up the
-// other warpgroup's shared-memory P writes); bf16 rows are stored from the row-per-thread
-// layout.
+// O_t of a finished short work item, drained partly through the (now idle) P_t buffer:
+// every thread loads its row and the tensor-memory buffer is released at once.  The P tile's
+// 32 KB hold the whole bf16 tile, or 64 fp32 columns; those are normalised and written to
+// P_t in the P tile's layout (128-byte-swizzled regions of 128 bytes per row), which is the
+// box layout of the output's tensor map, and one thread then stores them with TMA stores
+// (the softmax issues them once all rows are in).  Those stores drain at the SM's store rate
+// while the warpgroup computes the next item; P_t is written again only after they have read
+// it.  The remaining fp32 columns (D = 128) are stored first, directly, as in drain_o.
 template <int D, bool kOutF32>
-__device__ __forceinline__ void drain_o(const AttnParams& p, uint32_t tO, uint32_t o_empty_bar,
-                                        const Item& item, int t, int quarter, int lane,
-                                        float inv_l) {
+struct Staging {
+  static constexpr int kCols = kOutF32 ? (D < 64 ? D : 64) : D;  // columns staged in P_t
+  static constexpr int kBoxCols = kOutF32 ? 32 : 64;               // 128 bytes per row
+  static constexpr int kBoxes = kCols / kBoxCols;
+};
+
+template <int D, bool kOutF32>
+__device__ __forceinline__ void drain_o_staged(const AttnParams& p, uint32_t tO,
+                                               uint32_t o_empty_bar, uint32_t staged_bar,
+                                               uint32_t sP, const Item& item, int t, int quarter,
+                                               int lane, float inv_l) {
+  using L = AttnSmem<D>;
+  using S = Staging<D, kOutF32>;
   uint32_t o[D / 32][32];
   ptx::tc_fence_after();
 #pragma unroll
@@ -557,17 +570,17 @@ __device__ __forceinline__ void drain_o(const AttnParams& p, uint32_t tO, uint32
   ptx::tmem_wait_ld();
   ptx::tc_fence_before();
   ptx::mbar_arrive(o_empty_bar);  // the next item's first PV may overwrite O_t
-  const size_t out_off = item.out_off(p);
-  const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
-  if constexpr (kOutF32) {
+  const int r = quarter * 32 + lane;
+  if constexpr (kOutF32 && S::kCols < D) {
+    const size_t out_off = item.out_off(p);
+    const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
     const int r_lo = lane & 7, cgrp = lane >> 3;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = S::kCols / 32; c < D / 32; ++c) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * inv_l);
       swap_lane_reg_bit<4, 4>(o[c], lane);
       swap_lane_reg_bit<3, 3>(o[c], lane);
-      // o[c][8*rr + i] = (row row0w + 8*rr + r_lo, column 32*c + 8*cgrp + i)
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr) {
         const int row_k = row0w + rr * 8 + r_lo;
@@ -578,21 +591,32 @@ __device__ __forceinline__ void drain_o(const AttnParams& p, uint32_t tO, uint32
       }
     }
   } else {
-    const int row = row0w + lane;
-    if (row < p.n_q) {
-      __nv_bfloat16* dst = p.out_bf16 + out_off + static_cast<size_t>(row) * p.o_sn;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t wd[16];  // 32 columns of this thread's row as bf16 pairs
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          wd[i] = ptx::pack_bf16x2(__uint_as_float(o[c][2 * i]) * inv_l,
-                                   __uint_as_float(o[c][2 * i + 1]) * inv_l);
-        st_global_32B(dst + c * 32, p.out_align32, &wd[0]);
-        st_global_32B(dst + c * 32 + 16, p.out_align32, &wd[8]);
-      }
-    }
+    (void)p;
+    (void)item;
+    (void)t;
   }
+  const uint32_t sw = static_cast<uint32_t>(r & 7);
+  constexpr int kPerChunk = kOutF32 ? 4 : 8;  // elements per 16-byte chunk
+#pragma unroll
+  for (int ch = 0; ch < S::kCols / kPerChunk; ++ch) {
+    const uint32_t* x = &o[(ch * kPerChunk) / 32][(ch * kPerChunk) % 32];
+    uint32_t wv[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if constexpr (kOutF32)
+        wv[q] = __float_as_uint(__uint_as_float(x[q]) * inv_l);
+      else
+        wv[q] = ptx::pack_bf16x2(__uint_as_float(x[2 * q]) * inv_l,
+                                 __uint_as_float(x[2 * q + 1]) * inv_l);
+    }
+    const uint32_t addr =
+        sP + (ch / 8) * L::kRegion + r * 128 + ((static_cast<uint32_t>(ch % 8) ^ sw) << 4);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(wv[0]), "r"(wv[1]),
+                 "r"(wv[2]), "r"(wv[3])
+                 : "memory");
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::mbar_arrive(staged_bar);
 }
 
 template <int D, bool kOutF32, bool kAccum, bool kLse, bool kSoftDrain>
@@ -601,6 +625,8 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
                                            volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
+  // Short items drain O (partly, for fp32) through P_t with TMA stores (drain_o_staged).
+  constexpr bool kStaged = kSoftDrain;
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;  // row in the Q tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -726,6 +752,17 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
           if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, g);
           // The P_t buffer is free once PV_t(g-1) has read it.
           if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
+          if constexpr (kStaged) {
+            // ... and, at an item's first tile, once the previous item's staged O has been
+            // read out of it by the TMA stores.
+            if (j == 0 && li > 0) {
+              if (r == 0) {
+                ptx::bulk_wait_read_all();
+                ptx::mbar_arrive(bar(L::bStageFree + t));
+              }
+              if (!(ok = wait(L::bStageFree + t, (li - 1) & 1))) break;
+            }
+          }
         }
         // Pack to bf16 and store row r of this half's swizzled region; accumulate the row
         // sums (unrounded for the LSE, bf16-rounded for O) in independent chains.
@@ -783,7 +820,22 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
         (void)lse2;
       }
       if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
-      drain_o<D, kOutF32>(p, tO, bar(L::bOEmpty + t), item, t, quarter, lane, 1.f / lp);
+      if constexpr (kStaged) {
+        using S = Staging<D, kOutF32>;
+        drain_o_staged<D, kOutF32>(p, tO, bar(L::bOEmpty + t), bar(L::bStaged + t), sP, item, t,
+                                   quarter, lane, 1.f / lp);
+        if (quarter == 0) {
+          // All 128 rows staged: one thread stores them (rows past n_q are clipped).
+          if (!(ok = wait(L::bStaged + t, li & 1))) break;
+          if (lane == 0) {
+#pragma unroll
+            for (int rg = 0; rg < S::kBoxes; ++rg)
+              ptx::tma_store_5d(&p.tm_o, sP + rg * L::kRegion, rg * S::kBoxCols,
+                                item.q_row0 + t * kBlockM, item.h, item.b, item.split);
+            ptx::bulk_commit();
+          }
+        }
+      }
     } else if constexpr (!kAccum) {
       // Slot [t][r] = 1 / lp, reused once the epilogue has taken the previous item's value.
       if (li > 0 && !(ok = wait(L::bEpiTaken + t, (li - 1) & 1))) break;
@@ -811,6 +863,9 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     }
   }
   if (!ok) raise_abort(p, abort_flag);
+  if constexpr (kStaged) {
+    if (r == 0) ptx::bulk_wait_all();  // the last staged stores complete before the CTA exits
+  }
 }
 
 // Epilogue warpgroup (warps 12-15): for each work item and Q tile t, waits for the
@@ -1031,6 +1086,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(L::bOEmpty + t), kBlockM);
       ptx::mbar_init(bar(L::bEpiReady + t), kBlockM);
       ptx::mbar_init(bar(L::bEpiTaken + t), kBlockM);
+      ptx::mbar_init(bar(L::bStaged + t), kBlockM);
+      ptx::mbar_init(bar(L::bStageFree + t), 1);
     }
     ptx::mbar_init(bar(L::bDrainS), 1);
     ptx::mbar_init(bar(L::bDrainPV), 1);

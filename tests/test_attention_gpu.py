@@ -400,6 +400,40 @@ def test_persistent_grid_many_items_per_cta(limit):
         da.set_grid_limit(0)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_canaries_untouched_bf16_short_items(D):
+    """Short items with bf16 output store O with TMA stores clipped at the last query row:
+    outputs written through slices of larger buffers (fused, one chunk, all chunks in one
+    launch; ragged N) match the oracle and touch nothing outside."""
+    B, H, N, pad = 2, 2, 333, 4096
+    q, k, v = rand_qkv(B, H, N, D, seed=78 + D)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = to_dev(q, k, v)
+    n_out = B * H * N * D
+    big = torch.full((n_out + 2 * pad,), CANARY, device=DEV, dtype=torch.bfloat16)
+    out = big[pad:pad + n_out].view(B, H, N, D)
+    o, lse = da.attn_fwd(qd, kd, vd, out=out, scale=scale, out_dtype=torch.bfloat16)
+    one = torch.full((n_out + 2 * pad,), CANARY, device=DEV, dtype=torch.bfloat16)
+    oc, lc = da.attn_chunk_fwd(qd, kd[:, :, 100:300], vd[:, :, 100:300],
+                               out=one[pad:pad + n_out].view(B, H, N, D), scale=scale,
+                               out_dtype=torch.bfloat16)
+    chunks = (100, 133, 100)
+    parts = torch.full((3 * n_out + 2 * pad,), CANARY, device=DEV, dtype=torch.bfloat16)
+    P = parts[pad:pad + 3 * n_out].view(3, B, H, N, D)
+    _, L = da.attn_chunks_fwd(qd, kd, vd, chunks, partials=P, scale=scale,
+                              partial_dtype=torch.bfloat16)
+    da.check()
+    for buf, n in ((big, n_out), (one, n_out), (parts, 3 * n_out)):
+        assert (buf[:pad] == CANARY).all() and (buf[pad + n:] == CANARY).all()
+    assert_parity(o, lse, o_ref, lse_ref, f"D={D} bf16 short fused", bf16_out=True)
+    oc_ref, lc_ref = oracle.attention(q, k, v, scale, kv_start=100, kv_len=200)
+    assert_parity(oc, lc, oc_ref, lc_ref, f"D={D} bf16 short chunk", bf16_out=True)
+    om, lm = da.attn_lse_merge(P, L)
+    da.check()
+    assert_parity(om, lm, o_ref, lse_ref, f"D={D} bf16 short chunks merged", bf16_out=True)
+
+
 def outlier_qkv(B, H, N, D, seed):
     """CFG-stress-like inputs (the cfg workload's recipe at another shape): Q, K x gain and a
     fraction of keys x outlier gain, so the running max keeps rising and O is rescaled on most
