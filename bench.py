@@ -536,6 +536,19 @@ def run_gpu(args):
     da.check(dev)
     cross_ms = max_over_ranks(dist, x0.elapsed_time(x1) / nx)
     cross_flops = 4.0 * B * H * N * n_txt * D
+    # The same with bf16 output (what a DiT's cross-attention feeds its output projection).
+    out_x16 = torch.empty((B, H, N, D), device=dev, dtype=torch.bfloat16)
+    for _ in range(args.warmup):
+        da.attn_chunk_fwd(q, kx, vx, out=out_x16, lse=lse_c, scale=w.scale, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize(dev)
+    x0.record(stream)
+    for _ in range(nx):
+        da.attn_chunk_fwd(q, kx, vx, out=out_x16, lse=lse_c, scale=w.scale, out_dtype=torch.bfloat16)
+    x1.record(stream)
+    torch.cuda.synchronize(dev)
+    da.check(dev)
+    cross16_ms = max_over_ranks(dist, x0.elapsed_time(x1) / nx)
+    del out_x16
 
     # ---- end to end through the public API with host buffers ----
     q_p, k_p, v_p = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
@@ -667,8 +680,11 @@ def run_gpu(args):
                                    "unsplit_ms": stale_ms_unsplit,
                                    "unsplit_tflops": stale_flops / (stale_ms_unsplit * 1e-3)
                                    / 1e12},
-                "cross_attention_512_text_keys": {"ms": cross_ms,
+                "cross_attention_512_text_keys": {"ms": cross_ms, "out_dtype": "f32",
                                                   **tf_frac(cross_flops / (cross_ms * 1e-3) / 1e12)},
+                "cross_attention_512_text_keys_bf16_out": {
+                    "ms": cross16_ms, "out_dtype": "bf16",
+                    **tf_frac(cross_flops / (cross16_ms * 1e-3) / 1e12)},
                 "fused_vs_chunk_max_abs": diff,
             },
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128,fp32>",
