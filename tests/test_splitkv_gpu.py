@@ -96,6 +96,30 @@ def test_suggestion_and_capped_grid():
     check(o3, l3, o_ref, lse_ref, "split 7 on 3 CTAs")
 
 
+@pytest.mark.parametrize("limit", [0, 3])
+def test_short_ranges_staged_partials_on_capped_grid(limit):
+    """Split ranges of at most 16 key tiles take the short-item form, whose fp32 partials go
+    out through the partly staged TMA stores (the output map's range dimension): 16 ranges of
+    13-14 tiles over 27280 keys, the grid capped so that each CTA walks many items of
+    different ranges; ragged query count."""
+    B, H, Nq, N, D, S = 1, 3, 333, 27280, 128, 16
+    q = rand((B, H, Nq, D), seed=12)
+    k, v = rand((B, H, N, D), seed=13), rand((B, H, N, D), seed=14)
+    scale = 1 / math.sqrt(D)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    da.set_grid_limit(limit)
+    try:
+        o, lse = da.attn_chunk_fwd_splitkv(qd, kd, vd, scale=scale, splits=S)
+        ob, lb = da.attn_chunk_fwd_splitkv(qd, kd, vd, scale=scale, splits=S,
+                                           out_dtype=torch.bfloat16)
+        da.check()
+    finally:
+        da.set_grid_limit(0)
+    check(o, lse, o_ref, lse_ref, f"split {S} short ranges, grid {limit}")
+    check(ob, lb, o_ref, lse_ref, f"split {S} short ranges bf16 out, grid {limit}", bf16_out=True)
+
+
 def test_stale_kv_with_splits():
     B, H, N, m, row0, D = 1, 4, 4096, 512, 1024, 128
     k_buf, v_buf = rand((B, H, N, D), seed=7), rand((B, H, N, D), seed=8)
