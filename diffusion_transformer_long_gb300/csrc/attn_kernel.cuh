@@ -548,7 +548,9 @@ __device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uin
 // box layout of the output's tensor map, and one thread then stores them with TMA stores
 // (the softmax issues them once all rows are in).  Those stores drain at the SM's store rate
 // while the warpgroup computes the next item; P_t is written again only after they have read
-// it.  The remaining fp32 columns (D = 128) are stored first, directly, as in drain_o.
+// it.  The remaining fp32 columns (D = 128) are stored first, directly: two butterfly stages
+// of warp shuffles (lane bits 4,3 <-> register bits 4,3 of each 32-column chunk) make one
+// warp store cover 8 rows x 128 contiguous bytes, as in the epilogue warpgroup's stores.
 template <int D, bool kOutF32>
 struct Staging {
   static constexpr int kCols = kOutF32 ? (D < 64 ? D : 64) : D;  // columns staged in P_t
@@ -625,8 +627,6 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
                                            volatile int* abort_flag) {
   using L = AttnSmem<D>;
   auto bar = [&](int i) { return sbase + L::kBars + 8u * i; };
-  // Short items drain O (partly, for fp32) through P_t with TMA stores (drain_o_staged).
-  constexpr bool kStaged = kSoftDrain;
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;  // row in the Q tile == TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -752,7 +752,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
           if (r == 0) DIT_TRACE(kTrSmExp0 + 5 * t, g);
           // The P_t buffer is free once PV_t(g-1) has read it.
           if (!pv_prev_done && !(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
-          if constexpr (kStaged) {
+          if constexpr (kSoftDrain) {
             // ... and, at an item's first tile, once the previous item's staged O has been
             // read out of it by the TMA stores.
             if (j == 0 && li > 0) {
@@ -812,7 +812,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     float* const lse_row = p.lse + item.lse_off(p) + row;
     if constexpr (kSoftDrain) {
       // Short items: this warpgroup drains its own O_t once the item's last PV has landed
-      // (drain_o), instead of handing it to the epilogue warpgroup.
+      // (drain_o_staged), instead of handing it to the epilogue warpgroup.
       if constexpr (kLse) {
         if (row < p.n_q) *lse_row = lse2 * kLn2;
       } else {
@@ -820,7 +820,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
         (void)lse2;
       }
       if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
-      if constexpr (kStaged) {
+      if constexpr (kSoftDrain) {
         using S = Staging<D, kOutF32>;
         drain_o_staged<D, kOutF32>(p, tO, bar(L::bOEmpty + t), bar(L::bStaged + t), sP, item, t,
                                    quarter, lane, 1.f / lp);
@@ -863,7 +863,7 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     }
   }
   if (!ok) raise_abort(p, abort_flag);
-  if constexpr (kStaged) {
+  if constexpr (kSoftDrain) {
     if (r == 0) ptx::bulk_wait_all();  // the last staged stores complete before the CTA exits
   }
 }
