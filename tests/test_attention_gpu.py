@@ -434,6 +434,30 @@ def test_canaries_untouched_bf16_short_items(D):
     assert_parity(om, lm, o_ref, lse_ref, f"D={D} bf16 short chunks merged", bf16_out=True)
 
 
+def test_concurrent_launches_on_two_streams():
+    """A fused pass and a batched chunk pass launched at the same time on two streams (their
+    CTAs share the SMs): both results are bitwise those of the launches run one after the
+    other."""
+    w = synth.WORKLOADS["flux"]
+    q, k, v = to_dev(*synth.make_qkv(w))
+    o_ref, l_ref = da.attn_fwd(q, k, v, scale=w.scale)
+    p_ref, pl_ref = da.attn_chunks_fwd(q, k, v, w.chunks, scale=w.scale)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(s1):
+            o, l = da.attn_fwd(q, k, v, scale=w.scale)
+        with torch.cuda.stream(s2):
+            pp, pl = da.attn_chunks_fwd(q, k, v, w.chunks, scale=w.scale)
+        outs.append((o, l, pp, pl))
+    torch.cuda.synchronize()
+    da.check()
+    for o, l, pp, pl in outs:
+        assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+        assert torch.equal(pp, p_ref) and torch.equal(pl, pl_ref)
+
+
 def outlier_qkv(B, H, N, D, seed):
     """CFG-stress-like inputs (the cfg workload's recipe at another shape): Q, K x gain and a
     fraction of keys x outlier gain, so the running max keeps rising and O is rescaled on most
