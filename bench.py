@@ -18,6 +18,7 @@ has) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -87,21 +88,25 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 50 ms) of SM clock, power and throttle reasons; summary()
+    keeps the samples taken between mark_start() and mark_end() (the timed region).  The
+    driver refreshes its readings about every 100 ms, so each value appears about twice."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, device_index: int):
         self.proc = None
         self.out = None
+        self.t_start = self.t_end = None
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
         except Exception:
             ident = str(device_index)
         self.cmd = ["nvidia-smi", f"--id={ident}", f"--query-gpu={self.FIELDS}",
-                    "--format=csv,noheader,nounits", "-lms", "200"]
+                    "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)]
 
     def __enter__(self):
         try:
@@ -112,8 +117,15 @@ class ClockSampler:
         time.sleep(0.3)
         return self
 
+    def mark_start(self):
+        self.t_start = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t_end = datetime.datetime.now()
+
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.1)  # the sample covering the region's end
             self.proc.terminate()
             try:
                 self.out, _ = self.proc.communicate(timeout=5)
@@ -121,36 +133,53 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
-    def summary(self):
-        if not self.out:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+    def rows(self):
+        """(time, sm MHz, max MHz, watts or None, [active, hw, hw_thermal, sw_thermal, power_cap])
+        for every parsed sample."""
         rows = []
-        for line in self.out.strip().splitlines():
+        for line in (self.out or "").strip().splitlines():
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) != 8:
+            if len(parts) != 9:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-        if not rows:
+            try:
+                watts = float(parts[3])
+            except ValueError:
+                watts = None
+            rows.append((when, sm, mx, watts, parts[4:]))
+        return rows
+
+    def summary(self):
+        rows = self.rows()
+        if self.t_start is not None and self.t_end is not None:
+            inside = [r for r in rows if self.t_start <= r[0] <= self.t_end]
+            window = "inside the timed region"
+            if not inside:  # a region shorter than the sampling period
+                inside = [min(rows, key=lambda r: abs((r[0] - self.t_end).total_seconds()))] \
+                    if rows else []
+                window = "the sample nearest the timed region's end"
+        else:
+            inside, window = rows, "whole run"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
-                 "sw_power_cap"]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
-        for r in rows:
-            for n, v in zip(names[1:], r[3][1:]):
+        for r in inside:
+            for n, v in zip(names, r[4][1:]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
-        watts = []
-        for r in rows:
-            try:
-                watts.append(float(r[2]))
-            except ValueError:
-                pass
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows),
+        watts = [r[3] for r in inside if r[3] is not None]
+        sm = [r[1] for r in inside]
+        sm_max = max(r[2] for r in inside)
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": sm_max,
+                "frac_samples_below_max": sum(x < sm_max for x in sm) / len(sm),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "sampling": f"nvidia-smi every {self.PERIOD_MS} ms, {window}",
                 "power_w_max": max(watts) if watts else None}
 
 
@@ -315,6 +344,7 @@ def run_gpu(args):
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         barrier(dist)
         torch.cuda.synchronize(dev)
+        clk.mark_start()
         t0, t1 = ev(), ev()
         if flush is None:
             t0.record(stream)
@@ -333,6 +363,7 @@ def run_gpu(args):
                 s1.record(stream)
                 torch.cuda.synchronize(dev)
                 elapsed_ms += s0.elapsed_time(s1)
+        clk.mark_end()
         barrier(dist)
     da.check(dev)
     ms_step = max_over_ranks(dist, elapsed_ms / args.steps)
@@ -707,8 +738,13 @@ def run_gpu(args):
                          "achieved": fused_tflops, "peak": peak_burst, "unit": "TFLOP/s",
                          "frac": fused_tflops / peak_burst,
                          "peak_kind": f"{peak_src} bf16 burst (the timed region is under a "
-                                      f"second at the sampled clocks below)",
+                                      f"second; its sampled clocks are below)",
                          "frac_of_sustained_peak": fused_tflops / peak_sust,
+                         # The burst peak scaled by the median SM clock sampled inside the
+                         # timed region: the power cap lowers the clock under sustained load.
+                         "frac_at_sampled_clock": (
+                             fused_tflops / (peak_burst * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+                             if clocks.get("sm_mhz") and clocks.get("sm_max_mhz") else None),
                          "traffic": traffic,
                          "algorithmic_bytes": 3 * B * H * N * D * 2 + B * H * N * (D * 4 + 4)},
             "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
