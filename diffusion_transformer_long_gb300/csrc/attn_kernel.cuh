@@ -56,6 +56,8 @@
 // either way: O / l and m + log2 l do not depend on which m was used.
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_bf16.h>
 #include <cstdint>
 
@@ -541,67 +543,48 @@ __device__ __forceinline__ void st_global_32B(void* dst, bool align32, const uin
   }
 }
 
-// O_t of a finished short work item, drained partly through the (now idle) P_t buffer:
-// every thread loads its row and the tensor-memory buffer is released at once.  The P tile's
-// 32 KB hold the whole bf16 tile, or 64 fp32 columns; those are normalised and written to
-// P_t in the P tile's layout (128-byte-swizzled regions of 128 bytes per row), which is the
-// box layout of the output's tensor map, and one thread then stores them with TMA stores
-// (the softmax issues them once all rows are in).  Those stores drain at the SM's store rate
-// while the warpgroup computes the next item; P_t is written again only after they have read
-// it.  The remaining fp32 columns (D = 128) are stored first, directly: two butterfly stages
-// of warp shuffles (lane bits 4,3 <-> register bits 4,3 of each 32-column chunk) make one
-// warp store cover 8 rows x 128 contiguous bytes, as in the epilogue warpgroup's stores.
+// O_t of a finished short work item, drained through the (now idle) P_t buffer: every
+// thread loads its row and the tensor-memory buffer is released at once.  The P tile's 32 KB
+// hold the whole bf16 tile, or 64 fp32 columns: the rows are normalised and written to P_t
+// in the P tile's layout (128-byte-swizzled regions of 128 bytes per row), which is the box
+// layout of the output's tensor map, and one thread stores them with TMA stores once all
+// rows are in.  An fp32 tile of D = 128 goes in two rounds of 64 columns: the second is
+// written once the first round's stores have read P_t.  The stores drain at the SM's store
+// rate while the warpgroup goes on; P_t is written again only after they have read it.
 template <int D, bool kOutF32>
 struct Staging {
-  static constexpr int kCols = kOutF32 ? (D < 64 ? D : 64) : D;  // columns staged in P_t
+  static constexpr int kCols = kOutF32 ? (D < 64 ? D : 64) : D;  // columns per round
+  static constexpr int kRounds = D / kCols;
   static constexpr int kBoxCols = kOutF32 ? 32 : 64;               // 128 bytes per row
-  static constexpr int kBoxes = kCols / kBoxCols;
+  static constexpr int kBoxes = kCols / kBoxCols;                  // boxes per round
 };
 
-template <int D, bool kOutF32>
-__device__ __forceinline__ void drain_o_staged(const AttnParams& p, uint32_t tO,
-                                               uint32_t o_empty_bar, uint32_t staged_bar,
-                                               uint32_t sP, const Item& item, int t, int quarter,
-                                               int lane, float inv_l) {
-  using L = AttnSmem<D>;
-  using S = Staging<D, kOutF32>;
-  uint32_t o[D / 32][32];
+// All of O_t into registers (o[c] = columns 32c..32c+31 of this thread's row), then O_t
+// released to the next item's first PV.
+template <int D>
+__device__ __forceinline__ void load_o_release(uint32_t tO, uint32_t o_empty_bar,
+                                               uint32_t (&o)[D / 32][32]) {
   ptx::tc_fence_after();
 #pragma unroll
   for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + c * 32, o[c]);
   ptx::tmem_wait_ld();
   ptx::tc_fence_before();
-  ptx::mbar_arrive(o_empty_bar);  // the next item's first PV may overwrite O_t
-  const int r = quarter * 32 + lane;
-  if constexpr (kOutF32 && S::kCols < D) {
-    const size_t out_off = item.out_off(p);
-    const int row0w = item.q_row0 + t * kBlockM + quarter * 32;  // first row of this warp
-    const int r_lo = lane & 7, cgrp = lane >> 3;
-#pragma unroll
-    for (int c = S::kCols / 32; c < D / 32; ++c) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) o[c][i] = __float_as_uint(__uint_as_float(o[c][i]) * inv_l);
-      swap_lane_reg_bit<4, 4>(o[c], lane);
-      swap_lane_reg_bit<3, 3>(o[c], lane);
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int row_k = row0w + rr * 8 + r_lo;
-        if (row_k < p.n_q)
-          st_global_32B(p.out_f32 + out_off + static_cast<size_t>(row_k) * p.o_sn + c * 32 +
-                            cgrp * 8,
-                        p.out_align32, &o[c][rr * 8]);
-      }
-    }
-  } else {
-    (void)p;
-    (void)item;
-    (void)t;
-  }
+  ptx::mbar_arrive(o_empty_bar);
+}
+
+// Round `round` of the staging: columns [round * kCols, (round + 1) * kCols) of row r,
+// scaled by inv_l, into P_t; then the generic-proxy writes are made visible to the TMA.
+template <int D, bool kOutF32, int kRound>
+__device__ __forceinline__ void stage_o(const uint32_t (&o)[D / 32][32], uint32_t sP, int r,
+                                        float inv_l) {
+  using L = AttnSmem<D>;
+  using S = Staging<D, kOutF32>;
   const uint32_t sw = static_cast<uint32_t>(r & 7);
   constexpr int kPerChunk = kOutF32 ? 4 : 8;  // elements per 16-byte chunk
+  constexpr int kCol0 = kRound * S::kCols;
 #pragma unroll
   for (int ch = 0; ch < S::kCols / kPerChunk; ++ch) {
-    const uint32_t* x = &o[(ch * kPerChunk) / 32][(ch * kPerChunk) % 32];
+    const uint32_t* x = &o[(kCol0 + ch * kPerChunk) / 32][(kCol0 + ch * kPerChunk) % 32];
     uint32_t wv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -618,7 +601,6 @@ __device__ __forceinline__ void drain_o_staged(const AttnParams& p, uint32_t tO,
                  : "memory");
   }
   ptx::fence_proxy_async_smem();
-  ptx::mbar_arrive(staged_bar);
 }
 
 template <int D, bool kOutF32, bool kAccum, bool kLse, bool kSoftDrain>
@@ -760,7 +742,9 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
                 ptx::bulk_wait_read_all();
                 ptx::mbar_arrive(bar(L::bStageFree + t));
               }
-              if (!(ok = wait(L::bStageFree + t, (li - 1) & 1))) break;
+              if (!(ok = wait(L::bStageFree + t,
+                              Staging<D, kOutF32>::kRounds == 2 ? 1 : (li - 1) & 1)))
+                break;
             }
           }
         }
@@ -812,7 +796,8 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
     float* const lse_row = p.lse + item.lse_off(p) + row;
     if constexpr (kSoftDrain) {
       // Short items: this warpgroup drains its own O_t once the item's last PV has landed
-      // (drain_o_staged), instead of handing it to the epilogue warpgroup.
+      // (through P_t: load_o_release, stage_o), instead of handing it to the epilogue
+      // warpgroup.
       if constexpr (kLse) {
         if (row < p.n_q) *lse_row = lse2 * kLn2;
       } else {
@@ -822,18 +807,38 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
       if (!(ok = wait(L::bPVDone + t, (g - 1) & 1))) break;
       if constexpr (kSoftDrain) {
         using S = Staging<D, kOutF32>;
-        drain_o_staged<D, kOutF32>(p, tO, bar(L::bOEmpty + t), bar(L::bStaged + t), sP, item, t,
-                                   quarter, lane, 1.f / lp);
-        if (quarter == 0) {
-          // All 128 rows staged: one thread stores them (rows past n_q are clipped).
-          if (!(ok = wait(L::bStaged + t, li & 1))) break;
-          if (lane == 0) {
+        const float inv_l = 1.f / lp;
+        uint32_t o[D / 32][32];
+        load_o_release<D>(tO, bar(L::bOEmpty + t), o);
+        // Per item, STAGED completes once per round and STAGE_FREE once per round: after
+        // round 0's stores have read P_t (two rounds), and before the next item's first P
+        // write.  With two rounds their phases alternate within the item.
+        auto stage_and_store = [&](auto round_tag) -> bool {
+          constexpr int kRound = decltype(round_tag)::value;
+          stage_o<D, kOutF32, kRound>(o, sP, r, inv_l);
+          ptx::mbar_arrive(bar(L::bStaged + t));
+          if (quarter == 0) {
+            // All 128 rows staged: one thread stores them (rows past n_q are clipped).
+            if (!wait(L::bStaged + t, S::kRounds == 2 ? kRound : (li & 1))) return false;
+            if (lane == 0) {
 #pragma unroll
-            for (int rg = 0; rg < S::kBoxes; ++rg)
-              ptx::tma_store_5d(&p.tm_o, sP + rg * L::kRegion, rg * S::kBoxCols,
-                                item.q_row0 + t * kBlockM, item.h, item.b, item.split);
-            ptx::bulk_commit();
+              for (int rg = 0; rg < S::kBoxes; ++rg)
+                ptx::tma_store_5d(&p.tm_o, sP + rg * L::kRegion, kRound * S::kCols + rg * S::kBoxCols,
+                                  item.q_row0 + t * kBlockM, item.h, item.b, item.split);
+              ptx::bulk_commit();
+            }
           }
+          return true;
+        };
+        if (!(ok = stage_and_store(std::integral_constant<int, 0>{}))) break;
+        if constexpr (S::kRounds == 2) {
+          // P_t takes the second half once the first half's stores have read it.
+          if (r == 0) {
+            ptx::bulk_wait_read_all();
+            ptx::mbar_arrive(bar(L::bStageFree + t));
+          }
+          if (!(ok = wait(L::bStageFree + t, 0))) break;
+          if (!(ok = stage_and_store(std::integral_constant<int, 1>{}))) break;
         }
       }
     } else if constexpr (!kAccum) {
