@@ -810,9 +810,10 @@ __device__ __forceinline__ void softmax_wg(const AttnParams& p, uint32_t sbase, 
         const float inv_l = 1.f / lp;
         uint32_t o[D / 32][32];
         load_o_release<D>(tO, bar(L::bOEmpty + t), o);
-        // Per item, STAGED completes once per round and STAGE_FREE once per round: after
-        // round 0's stores have read P_t (two rounds), and before the next item's first P
-        // write.  With two rounds their phases alternate within the item.
+        // STAGED completes once per round.  STAGE_FREE completes before the next item's first
+        // P write and, with two rounds, also between them (once round 0's stores have read
+        // P_t).  With two rounds both complete twice per item, so the parity of each wait is
+        // fixed: 0 for the first completion, 1 for the second.
         auto stage_and_store = [&](auto round_tag) -> bool {
           constexpr int kRound = decltype(round_tag)::value;
           stage_o<D, kOutF32, kRound>(o, sP, r, inv_l);
