@@ -220,6 +220,29 @@ def test_cross_attention_512_keys_full_shape(out_dtype):
                   bf16_out=out_dtype == torch.bfloat16)
 
 
+def test_two_million_keys_ragged():
+    """A sequence far longer than the pages' workloads: N = 2^21 + 37 tokens (8193 query pairs
+    and key tiles per head, a 37-key ragged tail), D = 64, fused and as 3 uneven chunks merged
+    by LSE; sampled rows (first/last 16 included) against the oracle."""
+    n = (1 << 21) + 37
+    c0, c1 = 700_001, 650_000
+    w = synth.Workload("long2m", 1, 1, n, 64, 11, "iid", (c0, c1, n - c0 - c1))
+    q, k, v = synth.make_qkv(w)
+    rows = synth.sample_rows(n, 48, seed=w.seed)
+    o_ref, lse_ref = oracle.attention(q, k, v, w.scale, rows=rows)
+    qd, kd, vd = to_dev(q, k, v)
+    del q, k, v
+    o, lse = da.attn_fwd(qd, kd, vd, scale=w.scale)
+    da.check()
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, "fused 2M")
+    del o, lse
+    o, lse = da.chunk_attention(qd, kd, vd, list(w.chunks), scale=w.scale, batched=True)
+    da.check()
+    assert_parity(*pick(o, lse, rows), o_ref, lse_ref, "3 chunks 2M")
+    del o, lse, qd, kd, vd
+    torch.cuda.empty_cache()
+
+
 # ----------------------------------------------------------------- closed forms / invariants
 @pytest.fixture(scope="module")
 def flux_inputs():
