@@ -16,8 +16,9 @@
 // Persistent: one CTA per SM walks work items (head bh, pair of 128-row Q tiles,
 // key range) w = blockIdx.x, blockIdx.x + gridDim.x, ...  (head-major, so the CTAs
 // resident at any moment share a head's K/V in L2; the key range is the whole key
-// set, a tile-aligned split, or one chunk at any row offset).  Every barrier's phase count runs on across items, so the
-// next item's Q load and first S MMAs overlap this item's epilogue.
+// set, a tile-aligned split, or one chunk at any row offset).  Every barrier's phase
+// count runs on across items, so the next item's Q load and first S MMAs overlap this
+// item's epilogue.
 //
 // CTA organisation (512 threads, four warpgroups):
 //   warps 0-3   softmax for Q tile 0   (thread = query row = TMEM lane)
@@ -27,7 +28,8 @@
 //   warp 10     single-thread issuer of O += P V       (warp 11 idle)
 //   warps 12-15 epilogue: O_t out of TMEM, normalised, stored; both Q tiles
 //               (kSoftDrain, for work items of few KV tiles: each softmax warpgroup drains
-//               its own O_t once the item's last PV has landed, and warps 12-15 idle)
+//               its own O_t once the item's last PV has landed, staging it through its
+//               P_t buffer for TMA stores, and warps 12-15 idle)
 // Two issuers keep the tensor pipe fed: its queue is about one instruction deep,
 // and a barrier wait stalls the waiting thread for longer than one MMA, so while
 // one issuer waits the other issues.
